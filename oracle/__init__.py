@@ -1,0 +1,138 @@
+"""fp64 CPU oracle for the APEX-1 attention block -- TEST INFRASTRUCTURE ONLY.
+
+The oracle is the yardstick the CUDA library is checked against.  Only the
+tests, the smoke check in ``__graft_entry__`` and the CPU-baseline leg of
+``bench.py`` may import it; the product package never does.  It shares no code
+with the CUDA path: the arithmetic lives in ``oracle.c`` (plain C, double
+precision), written from the formulas of "APEX-1 Mathematical Reference --
+Part 1" (§4 RoPE) and "-- Part 2" (§6 scaled dot-product attention, §8 GQA,
+§10 sliding window).  This module only compiles that file and marshals arrays.
+
+Every function here is pinned by ``tests/test_oracle.py`` against the pages'
+worked examples, closed forms, invariants and an independent brute force.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so (plain gcc, no -march)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-std=c99", "-D_POSIX_C_SOURCE=200809L", "-ffp-contract=off",
+               "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i32, i64, f64 = ctypes.c_int, ctypes.c_long, ctypes.c_double
+            vp = ctypes.c_void_p
+            lib.oracle_rope_f64.argtypes = [vp, vp, i64, i32, vp, f64]
+            lib.oracle_rope_f64.restype = i32
+            lib.oracle_rope_theta_f64.argtypes = [i32, f64, vp]
+            lib.oracle_rope_theta_f64.restype = i32
+            for name in ("oracle_attn_bf16", "oracle_attn_f64"):
+                fn = getattr(lib, name)
+                fn.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i64, f64, i32,
+                               vp, i32, i32]
+                fn.restype = i32
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def rope_theta(d: int, base: float = 10000.0) -> np.ndarray:
+    """theta_i = base^(-2i/d) for i < d/2 (Part 1, §4.3)."""
+    out = np.empty(d // 2, dtype=np.float64)
+    rc = _load().oracle_rope_theta_f64(d, float(base), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_rope_theta_f64: bad arguments")
+    return out
+
+
+def rope(x, pos, base: float = 10000.0) -> np.ndarray:
+    """RoPE of the rows of x[..., d] at positions pos (Part 1, §4.2-§4.4)."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    d = x.shape[-1]
+    flat = x.reshape(-1, d)
+    p = np.ascontiguousarray(np.broadcast_to(np.asarray(pos, dtype=np.int64), (flat.shape[0],)))
+    out = np.empty_like(flat)
+    rc = _load().oracle_rope_f64(_ptr(flat), _ptr(out), flat.shape[0], d, _ptr(p), float(base))
+    if rc != 0:
+        raise ValueError("oracle_rope_f64: bad arguments")
+    return out.reshape(x.shape)
+
+
+def _as_bf16_bits(t) -> np.ndarray:
+    """torch bf16 tensor (any device) -> contiguous uint16 numpy array of its bits."""
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16:
+        raise TypeError("expected a torch.bfloat16 tensor")
+    return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def attn(q, k, v, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.0,
+         causal: bool = True, rows=None, threads: int | None = None) -> np.ndarray:
+    """Attention block in fp64.
+
+    q [B, H_q, S_q, d]; k, v [B, H_kv, S_k, d].  bf16 torch tensors are read as
+    their exact bf16 values; anything else is taken as float64.  Returns
+    out [B, H_q, n_rows, d] (float64), n_rows = S_q or len(rows).
+    rope_base <= 0 disables RoPE; causal=False disables the mask (both only for
+    the unmasked worked example of Part 2, §6.4).
+    """
+    import torch
+    bf16 = isinstance(q, torch.Tensor) and q.dtype == torch.bfloat16
+    if bf16:
+        qa, ka, va = _as_bf16_bits(q), _as_bf16_bits(k), _as_bf16_bits(v)
+        fn = _load().oracle_attn_bf16
+    else:
+        cv = lambda a: np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+        qa, ka, va = cv(q), cv(k), cv(v)
+        fn = _load().oracle_attn_f64
+    B, H_q, S_q, d = qa.shape
+    Bk, H_kv, S_k, dk = ka.shape
+    if va.shape != ka.shape or Bk != B or dk != d:
+        raise ValueError("shape mismatch between q, k, v")
+    if rows is None:
+        rows_arr, n_rows, rows_ptr = None, S_q, None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+        n_rows, rows_ptr = int(rows_arr.shape[0]), _ptr(rows_arr)
+    out = np.empty((B, H_q, n_rows, d), dtype=np.float64)
+    rc = fn(_ptr(qa), _ptr(ka), _ptr(va), _ptr(out), B, H_q, H_kv, S_q, S_k, d, int(window),
+            int(q_pos0), float(rope_base), 1 if causal else 0, rows_ptr, n_rows,
+            int(threads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle_attn failed with code %d" % rc)
+    return out

@@ -1,0 +1,435 @@
+"""Benchmark of the APEX-1 attention hot path on GB300.
+
+One step = one pass of the whole hot path on synthetic, seeded bf16 inputs:
+  * apex_attn_fwd on the GQA prefill workload (B=4, H_q=32, H_kv=8, S=4096,
+    d_h=128, causal + window 1024): RoPE, QK^T, mask/skip, online softmax, PV;
+  * apex_attn_decode on the decode workload (B=64, H_q=32, H_kv=8, one query at
+    position 32767 against a 32768-entry bf16 KV cache, d_h=128): split-KV
+    kernel + log-sum-exp combine.
+
+Reported (one JSON line on rank 0):
+  value    prefill TFLOP/s over unmasked work, 4 * d_h * visible pairs * B * H_q
+           per call, timed with CUDA events around the prefill calls;
+  decode   KV GB/s, K + V bytes of the visible keys per call over the decode calls;
+  roofline for the kernel that dominates the step (the decode split kernel,
+           HBM-bound) and roofline_prefill (tensor-bound), against the measured
+           peaks in MEASURED_PEAKS.json;
+  e2e      the same two metrics through the same C-ABI calls with the inputs in
+           pinned host memory: every step copies the step's inputs host->device
+           and the outputs device->host inside the timed region;
+  cpu_baseline  the fp64 oracle, as it stands, on a bounded sample of the same
+           workloads on this machine's host cores.
+
+With --impl reference the oracle itself is the timed arm (host cores, bounded
+sample per step); it prints the same keys with "impl": "reference".
+Multi-GPU (torchrun): every rank runs the same step on its own GPU with its own
+seed (independent problems, no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s and decode KV GB/s on 1×GB300, as % of roofline"
+PREFILL = "gqa"
+DECODE = "decode"
+
+
+def visible_pairs(S_q, S_k, window, q_pos0):
+    """Number of (query, key) pairs the causal/window mask leaves visible, per head."""
+    total = 0
+    for r in range(S_q):
+        m = q_pos0 + r
+        lo = max(0, m - window + 1) if window > 0 else 0
+        total += min(m, S_k - 1) - lo + 1
+    return total
+
+
+def prefill_flops(w):
+    return 4.0 * w.d_h * visible_pairs(w.S_q, w.S_k, w.window, w.q_pos0) * w.B * w.H_q
+
+
+def decode_kv_bytes(w):
+    m = w.q_pos0
+    lo = max(0, m - w.window + 1) if w.window > 0 else 0
+    return 2.0 * w.B * w.H_kv * (m - lo + 1) * w.d_h * 2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id):
+        self.bus_id = bus_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "200"]
+            if self.bus_id:
+                cmd[1:1] = ["-i", self.bus_id]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = []
+        smax = None
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                smax = float(r[1])
+            except ValueError:
+                continue
+            for n, val in zip(names, r[4:8]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def bus_id_of(dev_index):
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev_index)
+        return "%08x:%02x:%02x.0" % (getattr(p, "pci_domain_id", 0), p.pci_bus_id, p.pci_device_id)
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- CPU baseline (oracle)
+def oracle_sample_prefill(w, q, k, v, budget_rows):
+    """Oracle on batch 0, all heads, an evenly spaced subset of rows."""
+    import oracle
+    step = max(1, w.S_q // budget_rows)
+    rows = list(range(0, w.S_q, step))
+    t0 = time.perf_counter()
+    oracle.attn(q[:1], k[:1], v[:1], window=w.window, q_pos0=w.q_pos0, rows=rows)
+    dt = time.perf_counter() - t0
+    pairs = 0
+    for r in rows:
+        m = w.q_pos0 + r
+        lo = max(0, m - w.window + 1) if w.window > 0 else 0
+        pairs += m - lo + 1
+    flops = 4.0 * w.d_h * pairs * w.H_q
+    return flops, dt, "prefill %s: batch 0 of %d, all %d heads, %d of %d rows (every %d-th)" % (
+        w.name, w.B, w.H_q, len(rows), w.S_q, step)
+
+
+def oracle_sample_decode(w, q, k, v, n_batch):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.attn(q[:n_batch], k[:n_batch], v[:n_batch], window=w.window, q_pos0=w.q_pos0)
+    dt = time.perf_counter() - t0
+    m = w.q_pos0
+    lo = max(0, m - w.window + 1) if w.window > 0 else 0
+    nbytes = 2.0 * n_batch * w.H_kv * (m - lo + 1) * w.d_h * 2
+    return nbytes, dt, "decode: %d of %d sequences, full cache" % (n_batch, w.B)
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(prefill_inputs, decode_inputs, rows=256, dec_batch=4):
+    from transformer_attention_rope_gb300 import inputs as inp
+    wp, wd = inp.WORKLOADS[PREFILL], inp.WORKLOADS[DECODE]
+    fl, dtp, sp = oracle_sample_prefill(wp, *prefill_inputs, rows)
+    nb, dtd, sd = oracle_sample_decode(wd, *decode_inputs, dec_batch)
+    return {"value": fl / dtp / 1e12, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+            "sample": "%s (%.1f s); %s (%.1f s)" % (sp, dtp, sd, dtd),
+            "decode_value": nb / dtd / 1e9, "decode_unit": "GB/s", "seconds": dtp + dtd}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from transformer_attention_rope_gb300 import inputs as inp
+    wp, wd = inp.WORKLOADS[PREFILL], inp.WORKLOADS[DECODE]
+    # inputs: the prefill workload in full, the decode workload for the sampled sequences only
+    pin = inp.workload_inputs(wp)
+    dq = inp.normal_bf16((wd.B, wd.H_q, 1, wd.d_h), wd.seed, 0)
+    n_dec = 2
+    dk = inp.normal_bf16((wd.B, wd.H_kv, wd.S_k, wd.d_h), wd.seed, 1)[:n_dec].contiguous()
+    dv = inp.normal_bf16((wd.B, wd.H_kv, wd.S_k, wd.d_h), wd.seed, 2)[:n_dec].contiguous()
+    rows = 32
+    for _ in range(args.warmup):
+        oracle_sample_prefill(wp, *pin, rows)
+    fl_tot = t_p = nb_tot = t_d = 0.0
+    sample = ""
+    for _ in range(args.steps):
+        fl, dt, sp = oracle_sample_prefill(wp, *pin, rows)
+        nb, dt2, sd = oracle_sample_decode(wd, dq[:n_dec].contiguous(), dk, dv, n_dec)
+        fl_tot += fl
+        t_p += dt
+        nb_tot += nb
+        t_d += dt2
+        sample = sp + "; " + sd
+    value = fl_tot / t_p / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": (t_p + t_d) * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill %s + decode %s (oracle sample)" % (PREFILL, DECODE)},
+        "decode": {"value": nb_tot / t_d / 1e9, "unit": "GB/s"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    import transformer_attention_rope_gb300 as apex
+    from transformer_attention_rope_gb300 import inputs as inp
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    apex.load_library()
+
+    wp, wd = inp.WORKLOADS[PREFILL], inp.WORKLOADS[DECODE]
+    # every rank gets its own seeds: independent problems
+    import dataclasses
+    wp = dataclasses.replace(wp, seed=wp.seed + 1000 * rank)
+    wd = dataclasses.replace(wd, seed=wd.seed + 1000 * rank)
+
+    pin = inp.workload_inputs(wp, pin=True)
+    din = inp.workload_inputs(dataclasses.replace(wd, S_q=1), pin=True)
+    pq, pk, pv = (t.to(dev, non_blocking=True) for t in pin)
+    dq, dk, dv = (t.to(dev, non_blocking=True) for t in din)
+    pout = torch.empty_like(pq)
+    dout = torch.empty_like(dq)
+    ws = torch.empty(apex.decode_workspace_bytes(wd.B, wd.H_q, wd.H_kv, wd.S_k, wd.d_h), dtype=torch.uint8,
+                     device=dev)
+    apex.apex_attn_rope_reserve(max(wp.S_k, wd.S_k), 128, 10000.0)
+    pout_h = torch.empty(pout.shape, dtype=pout.dtype, pin_memory=True)
+    dout_h = torch.empty(dout.shape, dtype=dout.dtype, pin_memory=True)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    def step():
+        apex.fwd(pq, pk, pv, window=wp.window, q_pos0=wp.q_pos0, out=pout)
+        apex.decode(dq, dk, dv, wd.q_pos0, window=wd.window, out=dout, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st = apex.apex_attn_device_status()
+    if st != 0:
+        raise RuntimeError("device status %d after warm-up" % st)
+
+    # ---- device-resident timed region
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(bus_id_of(local))
+    sampler.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        ev[i][0].record(stream)
+        apex.fwd(pq, pk, pv, window=wp.window, q_pos0=wp.q_pos0, out=pout)
+        ev[i][1].record(stream)
+        apex.decode(dq, dk, dv, wd.q_pos0, window=wd.window, out=dout, workspace=ws)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    t_pre = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
+    t_all = ev[0][0].elapsed_time(ev[-1][2]) / 1e3
+    st = apex.apex_attn_device_status()
+    if st != 0:
+        raise RuntimeError("device status %d after the timed region" % st)
+
+    # ---- end to end through the C ABI with pinned host buffers
+    h2d = sum(t.numel() * t.element_size() for t in (*pin, *din))
+    d2h = pout.numel() * pout.element_size() + dout.numel() * dout.element_size()
+    evx = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        evx[i][0].record(stream)
+        for dst, src in zip((pq, pk, pv), pin):
+            dst.copy_(src, non_blocking=True)
+        apex.fwd(pq, pk, pv, window=wp.window, q_pos0=wp.q_pos0, out=pout)
+        pout_h.copy_(pout, non_blocking=True)
+        evx[i][1].record(stream)
+        for dst, src in zip((dq, dk, dv), din):
+            dst.copy_(src, non_blocking=True)
+        apex.decode(dq, dk, dv, wd.q_pos0, window=wd.window, out=dout, workspace=ws)
+        dout_h.copy_(dout, non_blocking=True)
+        evx[i][2].record(stream)
+    torch.cuda.synchronize()
+    te_pre = sum(e[0].elapsed_time(e[1]) for e in evx) / 1e3
+    te_dec = sum(e[1].elapsed_time(e[2]) for e in evx) / 1e3
+
+    flops = prefill_flops(wp)
+    kvb = decode_kv_bytes(wd)
+    times = torch.tensor([t_pre, t_dec, t_all, te_pre, te_dec], dtype=torch.float64, device=dev)
+    if pg:
+        pg.all_reduce(times, op=pg.ReduceOp.MAX)
+    t_pre, t_dec, t_all, te_pre, te_dec = times.tolist()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(pin, din)
+
+    if rank == 0:
+        peaks = load_peaks()
+        pre_tflops = world * K * flops / t_pre / 1e12
+        dec_gbs = world * K * kvb / t_dec / 1e9
+        # per-launch figures of the kernels (one rank's launches)
+        pre_launch_s = t_pre / K
+        dec_launch_s = t_dec / K
+        dec_achieved = kvb / dec_launch_s / 1e9
+        pre_achieved = flops / pre_launch_s / 1e12
+        traffic = load_traffic()
+        line = {
+            "metric": METRIC,
+            "value": pre_tflops,
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": max(3, args.warmup),
+            "ms_per_step": t_all * 1e3 / K,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {
+                "workload": "prefill %s (B4 Hq32 Hkv8 S4096 d128 W1024) + decode %s (B64 Hq32 Hkv8 Sk32768 "
+                            "d128 q_pos 32767)" % (PREFILL, DECODE),
+                "prefill_tflop_per_call": flops / 1e12,
+                "decode_kv_bytes_per_call": kvb,
+                "l2": "inputs larger than L2: prefill Q+K+V 201 MB, decode K+V 8.6 GB streamed between prefills",
+                "parallelism": "replica per GPU (independent problems)" if world > 1 else "1 GPU",
+            },
+            "decode": {"value": dec_gbs, "unit": "GB/s", "ms_per_call": dec_launch_s * 1e3,
+                       "frac_of_hbm": dec_achieved / peaks["hbm_gbs"]},
+            "prefill": {"value": pre_tflops, "unit": "TFLOP/s", "ms_per_call": pre_launch_s * 1e3,
+                        "frac_of_bf16": pre_achieved / peaks["bf16_tflops"],
+                        "frac_of_bf16_sustained": pre_achieved / peaks["bf16_tflops_sustained"]},
+            "roofline": {"kernel": "decode_split_kernel (+ its combine kernel, timed together)",
+                         "bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": dec_achieved / peaks["hbm_gbs"], "traffic": traffic.get("decode"),
+                         "peak_source": peaks["source"]},
+            "roofline_prefill": {"kernel": "prefill_kernel", "bound": "tensor", "achieved": pre_achieved,
+                                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                 "frac": pre_achieved / peaks["bf16_tflops"], "traffic": traffic.get("prefill"),
+                                 "peak_source": peaks["source"] + " (burst)"},
+            "e2e": {"value": world * K * flops / te_pre / 1e12, "unit": "TFLOP/s",
+                    "decode_value": world * K * kvb / te_dec / 1e9, "decode_unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * K,
+            "clocks": clocks,
+            "wall_s_timed": t_wall,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line))
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+def load_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernels."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return {}
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: v.get("dram_bytes_per_launch") for k, v in d.items() if isinstance(v, dict)}
+    except (OSError, ValueError):
+        return {}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,140 @@
+/*
+ * apex_attn.h -- C ABI of the GB300 (sm_103a) APEX-1 attention block.
+ *
+ * The block computes, for every batch b, query head h and query row r
+ * (APEX-1 Mathematical Reference, Part 1 §4 and Part 2 §6, §8, §10):
+ *
+ *   m      = q_pos0 + r                       position of the query row
+ *   g      = floor(h / G),  G = H_q / H_kv    KV head shared by the group
+ *                                             (Part 2 §8.2; §8.4 example)
+ *   q'     = RoPE(q[b,h,r], m)                interleaved pairs (2i, 2i+1)
+ *   k'_j   = RoPE(k[b,g,j], j)                rotated by angle pos*theta_i,
+ *                                             theta_i = base^(-2i/d_h)
+ *                                             (Part 1 §4.2-§4.4)
+ *   out    = sum_j softmax_j(<q', k'_j> / sqrt(d_h)) v[b,g,j]
+ *            over the keys j visible from m   (Part 2 §6.2)
+ *   visible(m, j) <=> j <= m  and  (window <= 0  or  m - j < window)
+ *                                             (Part 2 §10.2)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are dense, row-major, bf16 (raw 16-bit patterns), in device
+ *   memory, with the 4-D attention layout [B, H, S, d_h] (Part 1 §1 "Tensor
+ *   Shape Convention").  Every pointer must be 16-byte aligned.
+ * - The caller owns every buffer it passes.  The library owns only a per-device
+ *   cache of RoPE cos/sin tables (fp32, built in double precision on the host),
+ *   allocated on first use and grown on demand.  A call that has to build or
+ *   grow that table allocates device memory and synchronises the device;
+ *   apex_attn_rope_reserve() builds it ahead of time.
+ * - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *   stream) and returns before it finishes.  Calls are thread-compatible:
+ *   concurrent calls on one device serialise on an internal lock while they
+ *   enqueue.
+ * - Supported: d_h in {64, 128}; H_q % H_kv == 0 with G = H_q / H_kv in
+ *   {1, 2, 4, 8, 16}; 1 <= S <= 2^24; q_pos0 >= 0 and q_pos0 + S_q <= S_k, so
+ *   that every query row sees at least its own key.
+ * - Arguments are validated before anything is launched: a rejected call
+ *   launches nothing and returns APEX_ERR_INVALID_ARG (bad value) or
+ *   APEX_ERR_UNSUPPORTED (valid but outside the supported set).  A CUDA
+ *   failure while enqueuing returns APEX_ERR_CUDA; the CUDA error state is left
+ *   as the runtime reports it.  No entry point prints, traps or exits.
+ * - Every wait inside the kernels is bounded in time.  A wait that gives up
+ *   records a code in a per-device status word and lets the kernel finish
+ *   (with unspecified output); apex_attn_device_status() reads and clears it.
+ */
+#ifndef APEX_ATTN_H
+#define APEX_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum apex_status {
+    APEX_OK = 0,
+    APEX_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or position */
+    APEX_ERR_UNSUPPORTED = 2,  /* valid arguments outside the supported set     */
+    APEX_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed             */
+    APEX_ERR_NO_MEMORY = 4,    /* the RoPE table could not be allocated          */
+    APEX_ERR_DEVICE_TIMEOUT = 5 /* a kernel's bounded wait gave up (see below)   */
+} apex_status;
+
+/* Opaque CUDA stream handle (same object as cudaStream_t / CUstream). */
+typedef struct CUstream_st *apex_stream_t;
+
+/*
+ * Prefill: attention of S_q query rows against S_k keys.
+ *
+ *   q   [B, H_q,  S_q, d_h]  bf16, read      (query row r sits at q_pos0 + r)
+ *   k   [B, H_kv, S_k, d_h]  bf16, read      (raw keys: RoPE is applied here,
+ *   v   [B, H_kv, S_k, d_h]  bf16, read       key j at position j)
+ *   out [B, H_q,  S_q, d_h]  bf16, written   (must not overlap q, k or v)
+ *   window     <= 0: causal only; > 0: key j visible iff 0 <= m - j < window
+ *   rope_base  RoPE base b of theta_i = b^(-2i/d_h) (10000 on the pages);
+ *              must be finite and > 0
+ *
+ * Cites: Part 2 §6.2 (SDPA), §8.2 (GQA), §10.2 (mask); Part 1 §4 (RoPE).
+ * Errors: see the conventions above.  Result: softmax in fp32 with exp2; Q, K
+ * are rotated in fp32 and rounded to bf16 for the tensor cores, as is P.
+ */
+apex_status apex_attn_fwd(const void *q, const void *k, const void *v, void *out,
+                          int B, int H_q, int H_kv, int S_q, int S_k, int d_h,
+                          int window, int q_pos0, float rope_base, apex_stream_t stream);
+
+/*
+ * Bytes of caller-provided device workspace apex_attn_decode needs for these
+ * sizes (the split-KV partial results).  Returns 0 when the sizes are invalid.
+ * The same sizes with any window / q_pos never need more.
+ */
+size_t apex_attn_decode_workspace_bytes(int B, int H_q, int H_kv, int S_k, int d_h);
+
+/*
+ * Decode: one query per sequence against a bf16 KV cache.
+ *
+ *   q       [B, H_q,  1,   d_h] bf16, read   (the query sits at position q_pos)
+ *   k_cache [B, H_kv, S_k, d_h] bf16, read   (raw keys, key j at position j)
+ *   v_cache [B, H_kv, S_k, d_h] bf16, read
+ *   out     [B, H_q,  1,   d_h] bf16, written
+ *   q_pos   0 <= q_pos < S_k; keys j > q_pos are masked (causal)
+ *   window  as for apex_attn_fwd
+ *   workspace, workspace_bytes: device scratch of at least
+ *           apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_h) bytes,
+ *           16-byte aligned, owned by the caller, not read before written.
+ *
+ * The result equals apex_attn_fwd with S_q = 1 and q_pos0 = q_pos (up to the
+ * order of fp32 sums).  The KV range is split across CTAs; each split writes
+ * a partial (max, sum, unnormalised output) and a log-sum-exp combine kernel
+ * merges them (Part 2 §6.2: softmax is invariant to the shift by the max).
+ * Cites: Part 2 §6.2, §7.4 (KV cache), §8.2, §10.2; Part 1 §4.
+ */
+apex_status apex_attn_decode(const void *q, const void *k_cache, const void *v_cache, void *out,
+                             int B, int H_q, int H_kv, int S_k, int d_h, int window, int q_pos,
+                             float rope_base, void *workspace, size_t workspace_bytes,
+                             apex_stream_t stream);
+
+/*
+ * Build (or grow) the RoPE cos/sin table of the current device so that
+ * positions [0, max_pos) are covered for this (d_h, rope_base).  Synchronous.
+ * Calling it before capturing a CUDA graph keeps the captured calls free of
+ * allocations.  Part 1 §4.7 (cos/sin cache computed once, reused).
+ */
+apex_status apex_attn_rope_reserve(int max_pos, int d_h, float rope_base);
+
+/*
+ * Read and clear the current device's status word, after synchronising the
+ * device.  APEX_OK when no kernel recorded a problem since the last call;
+ * APEX_ERR_DEVICE_TIMEOUT when a bounded wait gave up; APEX_ERR_CUDA when the
+ * synchronisation itself failed.
+ */
+apex_status apex_attn_device_status(void);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *apex_attn_status_string(apex_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* APEX_ATTN_H */

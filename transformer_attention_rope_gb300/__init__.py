@@ -1,1 +1,158 @@
-"""GB300-native APEX-1 attention block (RoPE + GQA + causal/sliding-window SDPA)."""
+"""GB300-native APEX-1 attention block: RoPE + GQA + causal/sliding-window SDPA.
+
+This package is a thin ctypes binding over the C ABI declared in
+``include/apex_attn.h`` (``_build/libapex_attn.so``).  It only marshals
+arguments: every step of the computation runs in the library's CUDA kernels.
+There is no CPU fallback -- if the library is missing, every call raises.
+
+Raw C-ABI names (pointers and sizes):
+    apex_attn_fwd, apex_attn_decode, apex_attn_decode_workspace_bytes,
+    apex_attn_rope_reserve, apex_attn_device_status, apex_attn_status_string
+Tensor conveniences (torch, bf16, contiguous, on the current CUDA device):
+    fwd(q, k, v, ...), decode(q, k_cache, v_cache, q_pos, ...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "ApexError", "library_path", "load_library", "apex_attn_fwd", "apex_attn_decode",
+    "apex_attn_decode_workspace_bytes", "apex_attn_rope_reserve", "apex_attn_device_status",
+    "apex_attn_status_string", "fwd", "decode", "decode_workspace_bytes",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libapex_attn.so")
+_lock = threading.Lock()
+_lib = None
+
+APEX_OK = 0
+_STATUS_NAMES = {0: "APEX_OK", 1: "APEX_ERR_INVALID_ARG", 2: "APEX_ERR_UNSUPPORTED", 3: "APEX_ERR_CUDA",
+                 4: "APEX_ERR_NO_MEMORY", 5: "APEX_ERR_DEVICE_TIMEOUT"}
+
+
+class ApexError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s (%s)" % (what, _STATUS_NAMES.get(status, status),
+                                                 apex_attn_status_string(status)))
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load the CUDA library; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError("libapex_attn.so is not built (run __graft_entry__.build() or "
+                                   "python transformer_attention_rope_gb300/build.py); there is no fallback")
+            lib = ctypes.CDLL(_LIB_PATH)
+            vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            lib.apex_attn_fwd.argtypes = [vp, vp, vp, vp] + [i32] * 8 + [f32, vp]
+            lib.apex_attn_fwd.restype = i32
+            lib.apex_attn_decode.argtypes = [vp, vp, vp, vp] + [i32] * 7 + [f32, vp, sz, vp]
+            lib.apex_attn_decode.restype = i32
+            lib.apex_attn_decode_workspace_bytes.argtypes = [i32] * 5
+            lib.apex_attn_decode_workspace_bytes.restype = sz
+            lib.apex_attn_rope_reserve.argtypes = [i32, i32, f32]
+            lib.apex_attn_rope_reserve.restype = i32
+            lib.apex_attn_device_status.argtypes = []
+            lib.apex_attn_device_status.restype = i32
+            lib.apex_attn_status_string.argtypes = [i32]
+            lib.apex_attn_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+# ------------------------------------------------------------------ raw C ABI
+def apex_attn_fwd(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, window, q_pos0, rope_base, stream) -> int:
+    return load_library().apex_attn_fwd(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, window, q_pos0,
+                                        rope_base, stream)
+
+
+def apex_attn_decode(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, window, q_pos, rope_base,
+                     workspace, workspace_bytes, stream) -> int:
+    return load_library().apex_attn_decode(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, window, q_pos,
+                                           rope_base, workspace, workspace_bytes, stream)
+
+
+def apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_h) -> int:
+    return load_library().apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_h)
+
+
+def apex_attn_rope_reserve(max_pos, d_h, rope_base) -> int:
+    return load_library().apex_attn_rope_reserve(max_pos, d_h, rope_base)
+
+
+def apex_attn_device_status() -> int:
+    return load_library().apex_attn_device_status()
+
+
+def apex_attn_status_string(status: int) -> str:
+    return load_library().apex_attn_status_string(int(status)).decode()
+
+
+# ------------------------------------------------------------------ torch conveniences
+def _check(t, name, ndim):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError("%s must be a CUDA bf16 tensor" % name)
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous %d-D tensor" % (name, ndim))
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def fwd(q, k, v, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.0, out=None, stream=None):
+    """Prefill. q [B,H_q,S_q,d], k/v [B,H_kv,S_k,d] (bf16, CUDA) -> out [B,H_q,S_q,d]."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, 4)
+    B, H_q, S_q, d = q.shape
+    _, H_kv, S_k, _ = k.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", 4)
+    st = apex_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H_q, H_kv, S_q, S_k, d,
+                       int(window), int(q_pos0), float(rope_base), _stream_handle(stream))
+    if st != APEX_OK:
+        raise ApexError(st, "apex_attn_fwd")
+    return out
+
+
+def decode_workspace_bytes(B, H_q, H_kv, S_k, d_h) -> int:
+    return int(apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_h))
+
+
+def decode(q, k_cache, v_cache, q_pos: int, *, window: int = 0, rope_base: float = 10000.0, out=None,
+           workspace=None, stream=None):
+    """Decode. q [B,H_q,1,d], caches [B,H_kv,S_k,d] (bf16, CUDA) -> out [B,H_q,1,d]."""
+    import torch
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, 4)
+    B, H_q, one, d = q.shape
+    _, H_kv, S_k, _ = k_cache.shape
+    if one != 1:
+        raise ValueError("decode takes one query per sequence")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", 4)
+    need = decode_workspace_bytes(B, H_q, H_kv, S_k, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = apex_attn_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), B, H_q, H_kv,
+                          S_k, d, int(window), int(q_pos), float(rope_base), workspace.data_ptr(),
+                          workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != APEX_OK:
+        raise ApexError(st, "apex_attn_decode")
+    return out

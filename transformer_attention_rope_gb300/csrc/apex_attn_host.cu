@@ -1,0 +1,371 @@
+// apex_attn_host.cu -- the C ABI of include/apex_attn.h: argument checks, the
+// per-device RoPE cos/sin table, TMA descriptors and kernel launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <vector>
+
+#include "../../include/apex_attn.h"
+#include "kernel_params.h"
+
+namespace apex {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSeq = 1 << 24;
+
+struct RopeTable {
+    int d_h;
+    float base;
+    float2 *dev;
+    int cap;  // positions held
+};
+
+struct DeviceState {
+    std::mutex mu;
+    bool ready = false;
+    int sm_count = 0;
+    uint32_t *status = nullptr;  // per-device status word
+    std::vector<RopeTable> tables;
+};
+
+DeviceState g_state[kMaxDevices];
+
+uint64_t wait_timeout_ns()
+{
+    static uint64_t v = [] {
+        const char *e = getenv("APEX_ATTN_WAIT_TIMEOUT_MS");
+        long ms = e ? atol(e) : 0;
+        if (ms <= 0) ms = 2000;
+        return (uint64_t)ms * 1000000ull;
+    }();
+    return v;
+}
+
+apex_status init_device(DeviceState &st, int dev)
+{
+    if (st.ready) return APEX_OK;
+    if (cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return APEX_ERR_CUDA;
+    if (cudaMalloc(&st.status, sizeof(uint32_t)) != cudaSuccess) return APEX_ERR_NO_MEMORY;
+    if (cudaMemset(st.status, 0, sizeof(uint32_t)) != cudaSuccess) return APEX_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return APEX_ERR_CUDA;
+    st.ready = true;
+    return APEX_OK;
+}
+
+// Part 1, §4.3 and §4.7: theta_i = base^(-2i/d_h) and the (cos, sin) cache of
+// m * theta_i for every position m, computed in double precision and stored as
+// fp32 pairs [cap][d_h/2].
+apex_status get_table(DeviceState &st, int d_h, float base, int need, RopeTableView *out)
+{
+    need = std::max(need, 128);
+    for (auto &t : st.tables) {
+        if (t.d_h == d_h && t.base == base && t.cap >= need) {
+            *out = RopeTableView{t.dev, t.cap};
+            return APEX_OK;
+        }
+    }
+    int cap = 4096;
+    while (cap < need) cap *= 2;
+    const int half = d_h / 2;
+    std::vector<float2> host((size_t)cap * half);
+    for (int i = 0; i < half; ++i) {
+        const double theta = pow((double)base, -2.0 * (double)i / (double)d_h);
+        for (int m = 0; m < cap; ++m) {
+            const double a = (double)m * theta;
+            host[(size_t)m * half + i] = make_float2((float)cos(a), (float)sin(a));
+        }
+    }
+    float2 *dev = nullptr;
+    if (cudaMalloc(&dev, host.size() * sizeof(float2)) != cudaSuccess) {
+        cudaGetLastError();
+        return APEX_ERR_NO_MEMORY;
+    }
+    if (cudaMemcpy(dev, host.data(), host.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaFree(dev);
+        return APEX_ERR_CUDA;
+    }
+    // replace a smaller table of the same (d_h, base); cudaFree waits for the
+    // device, so no kernel still reads the old one
+    for (auto it = st.tables.begin(); it != st.tables.end(); ++it) {
+        if (it->d_h == d_h && it->base == base) {
+            cudaFree(it->dev);
+            st.tables.erase(it);
+            break;
+        }
+    }
+    st.tables.push_back(RopeTable{d_h, base, dev, cap});
+    *out = RopeTableView{dev, cap};
+    return APEX_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 map over a dense [outer][rows][d_h] tensor, 128-byte swizzle, box
+// {64 dims, box_rows, box_outer}; out-of-range elements read as zero.
+bool make_map(CUtensorMap *m, const void *base, int d_h, int rows, int outer, int box_rows, int box_outer)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d_h, (cuuint64_t)rows, (cuuint64_t)outer};
+    cuuint64_t strides[2] = {(cuuint64_t)d_h * 2, (cuuint64_t)rows * d_h * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_outer};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16; }
+
+apex_status check_common(int B, int H_q, int H_kv, int S_k, int d_h, float base)
+{
+    if (B <= 0 || H_q <= 0 || H_kv <= 0 || S_k <= 0 || d_h <= 0) return APEX_ERR_INVALID_ARG;
+    if (H_q % H_kv != 0) return APEX_ERR_INVALID_ARG;
+    if (!(base > 0.f) || !isfinite(base)) return APEX_ERR_INVALID_ARG;
+    if (S_k > kMaxSeq) return APEX_ERR_UNSUPPORTED;
+    if (d_h != 64 && d_h != 128) return APEX_ERR_UNSUPPORTED;
+    if (!supported_group(H_q / H_kv)) return APEX_ERR_UNSUPPORTED;
+    if ((long long)B * H_q > (1ll << 30) || (long long)B * H_kv * (long long)S_k > (1ll << 40))
+        return APEX_ERR_UNSUPPORTED;
+    return APEX_OK;
+}
+
+DeviceState *current_state(int *dev_out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    *dev_out = dev;
+    return &g_state[dev];
+}
+
+// --- decode split choice: the KV range of each (b, kv-head) unit is cut into
+// n_split splits of whole 64-key stages; pick the count that minimises the
+// modelled time rounds * (stages per split + 1) on a persistent grid.
+struct SplitPlan {
+    int n_split, stages_per_split;
+};
+
+int decode_split_cap(int units, int n_stages)
+{
+    long cap = std::max(1l, 32768l / std::max(1, units));
+    cap = std::min<long>(cap, n_stages);
+    cap = std::min<long>(cap, kDecodeMaxSplit);
+    return (int)std::max(1l, cap);
+}
+
+SplitPlan plan_decode(int units, int n_stages, int capacity)
+{
+    const int cap = decode_split_cap(units, n_stages);
+    SplitPlan best{1, n_stages};
+    double best_cost = 1e300;
+    for (int ns = 1; ns <= cap; ++ns) {
+        const int sps = (n_stages + ns - 1) / ns;
+        const int real = (n_stages + sps - 1) / sps;
+        if (real != ns) continue;
+        const long items = (long)units * ns;
+        const long rounds = (items + capacity - 1) / capacity;
+        const double cost = (double)rounds * (sps + 1);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = SplitPlan{ns, sps};
+        }
+    }
+    return best;
+}
+
+int max_stages_for(int S_k) { return (S_k + kDecodeKeysPerStage - 1) / kDecodeKeysPerStage + 1; }
+
+}  // namespace
+}  // namespace apex
+
+using namespace apex;
+
+extern "C" {
+
+const char *apex_attn_status_string(apex_status s)
+{
+    switch (s) {
+    case APEX_OK: return "ok";
+    case APEX_ERR_INVALID_ARG: return "invalid argument";
+    case APEX_ERR_UNSUPPORTED: return "unsupported configuration";
+    case APEX_ERR_CUDA: return "CUDA error";
+    case APEX_ERR_NO_MEMORY: return "out of device memory";
+    case APEX_ERR_DEVICE_TIMEOUT: return "a kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+apex_status apex_attn_rope_reserve(int max_pos, int d_h, float rope_base)
+{
+    if (max_pos <= 0 || max_pos > kMaxSeq) return APEX_ERR_INVALID_ARG;
+    if (!(rope_base > 0.f) || !isfinite(rope_base)) return APEX_ERR_INVALID_ARG;
+    if (d_h != 64 && d_h != 128) return APEX_ERR_UNSUPPORTED;
+    int dev;
+    DeviceState *st = current_state(&dev);
+    if (!st) return APEX_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(st->mu);
+    apex_status s = init_device(*st, dev);
+    if (s != APEX_OK) return s;
+    RopeTableView tv;
+    return get_table(*st, d_h, rope_base, max_pos, &tv);
+}
+
+apex_status apex_attn_device_status(void)
+{
+    int dev;
+    DeviceState *st = current_state(&dev);
+    if (!st) return APEX_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(st->mu);
+    if (cudaDeviceSynchronize() != cudaSuccess) return APEX_ERR_CUDA;
+    if (!st->ready) return APEX_OK;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, st->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return APEX_ERR_CUDA;
+    if (v == 0) return APEX_OK;
+    if (cudaMemset(st->status, 0, sizeof(uint32_t)) != cudaSuccess) return APEX_ERR_CUDA;
+    return APEX_ERR_DEVICE_TIMEOUT;
+}
+
+size_t apex_attn_decode_workspace_bytes(int B, int H_q, int H_kv, int S_k, int d_h)
+{
+    if (check_common(B, H_q, H_kv, S_k, d_h, 10000.f) != APEX_OK) return 0;
+    const int units = B * H_kv;
+    const int ns = decode_split_cap(units, max_stages_for(S_k));
+    const size_t rows = (size_t)B * H_q * ns;
+    size_t bytes = rows * (size_t)d_h * sizeof(float);
+    bytes = (bytes + 15) & ~size_t(15);
+    return bytes + rows * sizeof(float2);
+}
+
+apex_status apex_attn_decode(const void *q, const void *k_cache, const void *v_cache, void *out, int B, int H_q,
+                             int H_kv, int S_k, int d_h, int window, int q_pos, float rope_base, void *workspace,
+                             size_t workspace_bytes, apex_stream_t stream)
+{
+    if (!q || !k_cache || !v_cache || !out || !workspace) return APEX_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
+        return APEX_ERR_INVALID_ARG;
+    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, rope_base);
+    if (s != APEX_OK) return s;
+    if (q_pos < 0 || q_pos >= S_k) return APEX_ERR_INVALID_ARG;
+    const size_t need = apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_h);
+    if (workspace_bytes < need) return APEX_ERR_INVALID_ARG;
+
+    int dev;
+    DeviceState *st = current_state(&dev);
+    if (!st) return APEX_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(st->mu);
+    s = init_device(*st, dev);
+    if (s != APEX_OK) return s;
+    RopeTableView tv;
+    s = get_table(*st, d_h, rope_base, S_k, &tv);
+    if (s != APEX_OK) return s;
+
+    DecodeLaunch L;
+    memset(&L, 0, sizeof L);
+    const int units = B * H_kv;
+    if (!make_map(&L.tm_k, k_cache, d_h, S_k, units, kDecodeKeysPerStage, 1) ||
+        !make_map(&L.tm_v, v_cache, d_h, S_k, units, kDecodeKeysPerStage, 1))
+        return APEX_ERR_CUDA;
+    DecodeParams &p = L.p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.out = static_cast<uint16_t *>(out);
+    const int ns_cap = decode_split_cap(units, max_stages_for(S_k));
+    p.ws_o = static_cast<float *>(workspace);
+    size_t o_bytes = (size_t)B * H_q * ns_cap * d_h * sizeof(float);
+    o_bytes = (o_bytes + 15) & ~size_t(15);
+    p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + o_bytes);
+    p.rope = tv;
+    p.wait = WaitCtl{st->status, wait_timeout_ns()};
+    p.B = B;
+    p.H_q = H_q;
+    p.H_kv = H_kv;
+    p.G = H_q / H_kv;
+    p.S_k = S_k;
+    p.d_h = d_h;
+    p.q_pos = q_pos;
+    p.k_lo = (window > 0) ? std::max(0, q_pos - window + 1) : 0;
+    p.stage0 = p.k_lo / kDecodeKeysPerStage;
+    p.n_stages = q_pos / kDecodeKeysPerStage - p.stage0 + 1;
+    const int capacity = decode_ctas_per_sm(d_h, p.G) * st->sm_count;
+    SplitPlan plan = plan_decode(units, p.n_stages, capacity);
+    p.n_split = plan.n_split;
+    p.stages_per_split = plan.stages_per_split;
+    p.n_items = units * p.n_split;
+    p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d_h));
+    L.grid = std::min(p.n_items, capacity);
+    if (launch_decode(L, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return APEX_ERR_CUDA;
+    return APEX_OK;
+}
+
+apex_status apex_attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
+                          int S_q, int S_k, int d_h, int window, int q_pos0, float rope_base, apex_stream_t stream)
+{
+    if (!q || !k || !v || !out) return APEX_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return APEX_ERR_INVALID_ARG;
+    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, rope_base);
+    if (s != APEX_OK) return s;
+    if (S_q <= 0 || q_pos0 < 0 || (long long)q_pos0 + S_q > (long long)S_k) return APEX_ERR_INVALID_ARG;
+
+    int dev;
+    DeviceState *st = current_state(&dev);
+    if (!st) return APEX_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(st->mu);
+    s = init_device(*st, dev);
+    if (s != APEX_OK) return s;
+    RopeTableView tv;
+    s = get_table(*st, d_h, rope_base, S_k, &tv);
+    if (s != APEX_OK) return s;
+
+    const int G = H_q / H_kv;
+    const int rows_per_head = 128 / G;
+    PrefillLaunch L;
+    memset(&L, 0, sizeof L);
+    if (!make_map(&L.tm_q, q, d_h, S_q, B * H_q, rows_per_head, G) ||
+        !make_map(&L.tm_o, out, d_h, S_q, B * H_q, rows_per_head, G) ||
+        !make_map(&L.tm_k, k, d_h, S_k, B * H_kv, 128, 1) || !make_map(&L.tm_v, v, d_h, S_k, B * H_kv, 128, 1))
+        return APEX_ERR_CUDA;
+    PrefillParams &p = L.p;
+    p.rope = tv;
+    p.wait = WaitCtl{st->status, wait_timeout_ns()};
+    p.B = B;
+    p.H_q = H_q;
+    p.H_kv = H_kv;
+    p.G = G;
+    p.S_q = S_q;
+    p.S_k = S_k;
+    p.d_h = d_h;
+    p.window = window > 0 ? window : 0;
+    p.q_pos0 = q_pos0;
+    p.rows_per_head = rows_per_head;
+    p.n_qblocks = (S_q + 2 * rows_per_head - 1) / (2 * rows_per_head);
+    p.n_work = B * H_kv * p.n_qblocks;
+    p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d_h));
+    L.grid = p.n_work;
+    if (launch_prefill(L, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return APEX_ERR_CUDA;
+    return APEX_OK;
+}
+
+}  // extern "C"

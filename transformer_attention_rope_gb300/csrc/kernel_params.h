@@ -1,0 +1,78 @@
+// kernel_params.h -- plain parameter blocks passed from the host library to
+// the kernels, and the launch entry points each kernel file provides.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace apex {
+
+// Codes a kernel may leave in the per-device status word.
+constexpr uint32_t kStatusWaitTimeout = 1;
+
+struct WaitCtl {
+    uint32_t *status;     // per-device status word (device memory)
+    uint64_t timeout_ns;  // bound on any single wait
+};
+
+// (cos, sin)(pos * theta_i) for pos in [0, max_pos), i in [0, d_h/2), fp32,
+// row-major [max_pos][d_h/2].
+struct RopeTableView {
+    const float2 *cs;
+    int max_pos;
+};
+
+// ----------------------------------------------------------------- decode
+constexpr int kDecodeKeysPerStage = 64;  // keys per pipeline stage
+constexpr int kDecodeMaxSplit = 4096;    // hard cap on KV splits per (b, kv-head)
+
+struct DecodeParams {
+    const uint16_t *q;  // [B, H_q, 1, d_h] bf16
+    uint16_t *out;      // [B, H_q, 1, d_h] bf16
+    float *ws_o;        // [B*H_q, n_split, d_h]  partial outputs (unnormalised)
+    float2 *ws_ml;      // [B*H_q, n_split]       partial (max (log2 units), sum)
+    RopeTableView rope;
+    WaitCtl wait;
+    int B, H_q, H_kv, G, S_k, d_h;
+    int q_pos;              // query position
+    int k_lo;               // first visible key
+    int stage0;             // first stage index (stage s covers keys [64 s, 64 s + 64))
+    int n_stages;           // stages per (b, kv-head)
+    int n_split;            // splits per (b, kv-head)
+    int stages_per_split;   // last split may have fewer
+    int n_items;            // B * H_kv * n_split
+    float scale_log2;       // log2(e) / sqrt(d_h)
+};
+
+struct DecodeLaunch {
+    CUtensorMap tm_k, tm_v;  // 3-D maps over [B*H_kv, S_k, d_h], box {64, 64, 1}, 128B swizzle
+    DecodeParams p;
+    int grid;                // CTAs of the split kernel (persistent)
+};
+
+cudaError_t launch_decode(const DecodeLaunch &L, cudaStream_t stream);
+int decode_ctas_per_sm(int d_h, int G);
+
+// ----------------------------------------------------------------- prefill
+struct PrefillParams {
+    RopeTableView rope;
+    WaitCtl wait;
+    int B, H_q, H_kv, G, S_q, S_k, d_h;
+    int window;     // <= 0: none
+    int q_pos0;
+    int rows_per_head;   // query positions per head in one 128-row M tile (128 / G)
+    int n_qblocks;       // position blocks per (b, kv-head); a block = 2 M tiles
+    int n_work;          // B * H_kv * n_qblocks
+    float scale_log2;    // log2(e) / sqrt(d_h)
+};
+
+struct PrefillLaunch {
+    CUtensorMap tm_q, tm_k, tm_v, tm_o;
+    PrefillParams p;
+    int grid;
+};
+
+cudaError_t launch_prefill(const PrefillLaunch &L, cudaStream_t stream);
+
+}  // namespace apex

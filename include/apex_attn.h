@@ -115,6 +115,37 @@ apex_status apex_attn_decode(const void *q, const void *k_cache, const void *v_c
                              apex_stream_t stream);
 
 /*
+ * Decode that allocates nothing, for callers that cannot allocate device
+ * memory when they call: an engine whose device memory is all handed out by
+ * its own pool at start-up (a cudaMalloc would fail, fragment the pool or
+ * synchronise the device), a plugin interface with a fixed signature and no
+ * workspace slot, or a latency-critical loop that cannot afford an
+ * allocation's synchronisation.  The APEX-1 pages have no counterpart of this
+ * entry point; it computes exactly what apex_attn_decode computes.
+ *
+ *   Arguments, layouts and results: as apex_attn_decode, without workspace.
+ *   Scratch: split-KV partials live in a 16 MiB file-scope device array and
+ *     the RoPE table in a 16 MiB one (positions < 32768); every GPU that loads
+ *     the library holds these 32 MiB until the process exits.  Nothing in them
+ *     has to start at zero: each call writes every partial it reads.
+ *   Limits (APEX_ERR_UNSUPPORTED beyond them): S_k <= 32768, d_h in {64, 128},
+ *     G in {1, 2, 4, 8, 16}, and B * H_q * (4 * d_h + 8) <= 16 MiB (one split);
+ *     larger B * H_q only lowers the number of KV splits the scratch allows.
+ *   Set-up: the first call on a device (and the first call with a new
+ *     (d_h, rope_base) pair) looks up the arrays' device addresses, builds the
+ *     RoPE table on `stream` and synchronises that stream; make that call before
+ *     capturing any CUDA graph.
+ *   Concurrency: all calls on a device share the arrays, so calls that may
+ *     overlap on the GPU (different streams without ordering between them) race
+ *     and must not be issued.  A kernel wait that times out is not recorded
+ *     (there is no status word without allocation); the output is then
+ *     unspecified.
+ */
+apex_status apex_attn_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                     int B, int H_q, int H_kv, int S_k, int d_h, int window, int q_pos,
+                                     float rope_base, apex_stream_t stream);
+
+/*
  * Build (or grow) the RoPE cos/sin table of the current device so that
  * positions [0, max_pos) are covered for this (d_h, rope_base).  Synchronous.
  * Calling it before capturing a CUDA graph keeps the captured calls free of

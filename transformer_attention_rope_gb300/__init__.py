@@ -6,7 +6,7 @@ arguments: every step of the computation runs in the library's CUDA kernels.
 There is no CPU fallback -- if the library is missing, every call raises.
 
 Raw C-ABI names (pointers and sizes):
-    apex_attn_fwd, apex_attn_decode, apex_attn_decode_workspace_bytes,
+    apex_attn_fwd, apex_attn_decode, apex_attn_decode_noalloc, apex_attn_decode_workspace_bytes,
     apex_attn_rope_reserve, apex_attn_device_status, apex_attn_status_string
 Tensor conveniences (torch, bf16, contiguous, on the current CUDA device):
     fwd(q, k, v, ...), decode(q, k_cache, v_cache, q_pos, ...)
@@ -18,7 +18,7 @@ import os
 import threading
 
 __all__ = [
-    "ApexError", "library_path", "load_library", "apex_attn_fwd", "apex_attn_decode",
+    "ApexError", "library_path", "load_library", "apex_attn_fwd", "apex_attn_decode", "apex_attn_decode_noalloc",
     "apex_attn_decode_workspace_bytes", "apex_attn_rope_reserve", "apex_attn_device_status",
     "apex_attn_status_string", "fwd", "decode", "decode_workspace_bytes",
 ]
@@ -58,6 +58,8 @@ def load_library():
             lib.apex_attn_fwd.restype = i32
             lib.apex_attn_decode.argtypes = [vp, vp, vp, vp] + [i32] * 7 + [f32, vp, sz, vp]
             lib.apex_attn_decode.restype = i32
+            lib.apex_attn_decode_noalloc.argtypes = [vp, vp, vp, vp] + [i32] * 7 + [f32, vp]
+            lib.apex_attn_decode_noalloc.restype = i32
             lib.apex_attn_decode_workspace_bytes.argtypes = [i32] * 5
             lib.apex_attn_decode_workspace_bytes.restype = sz
             lib.apex_attn_rope_reserve.argtypes = [i32, i32, f32]
@@ -80,6 +82,12 @@ def apex_attn_decode(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, window, q
                      workspace, workspace_bytes, stream) -> int:
     return load_library().apex_attn_decode(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, window, q_pos,
                                            rope_base, workspace, workspace_bytes, stream)
+
+
+def apex_attn_decode_noalloc(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, window, q_pos, rope_base,
+                             stream) -> int:
+    return load_library().apex_attn_decode_noalloc(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, window,
+                                                   q_pos, rope_base, stream)
 
 
 def apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_h) -> int:

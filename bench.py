@@ -151,7 +151,7 @@ def bus_id_of(dev_index):
 
 # ---------------------------------------------------------------- CPU baseline (oracle)
 def oracle_sample_prefill(w, q, k, v, budget_rows):
-    """Oracle on batch 0, all heads, an evenly spaced subset of rows."""
+    """Oracle on batch 0, all heads, an evenly spaced subset of rows (all rows when budget_rows >= S_q)."""
     import oracle
     step = max(1, w.S_q // budget_rows)
     rows = list(range(0, w.S_q, step))
@@ -186,7 +186,7 @@ def cores_used():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(prefill_inputs, decode_inputs, rows=256, dec_batch=4):
+def cpu_baseline(prefill_inputs, decode_inputs, rows=4096, dec_batch=32):
     from transformer_attention_rope_gb300 import inputs as inp
     wp, wd = inp.WORKLOADS[PREFILL], inp.WORKLOADS[DECODE]
     fl, dtp, sp = oracle_sample_prefill(wp, *prefill_inputs, rows)
@@ -240,6 +240,8 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- our arm
 def run_ours(args):
+    import dataclasses
+
     import torch
 
     import transformer_attention_rope_gb300 as apex
@@ -255,38 +257,48 @@ def run_ours(args):
         pg = dist
     apex.load_library()
 
-    wp, wd = inp.WORKLOADS[PREFILL], inp.WORKLOADS[DECODE]
+    wp, wd = inp.WORKLOADS[args.prefill_workload], inp.WORKLOADS[DECODE]
+    do_pre, do_dec = args.part in ("all", "prefill"), args.part in ("all", "decode")
     # every rank gets its own seeds: independent problems
-    import dataclasses
     wp = dataclasses.replace(wp, seed=wp.seed + 1000 * rank)
     wd = dataclasses.replace(wd, seed=wd.seed + 1000 * rank)
-
-    pin = inp.workload_inputs(wp, pin=True)
-    din = inp.workload_inputs(dataclasses.replace(wd, S_q=1), pin=True)
-    pq, pk, pv = (t.to(dev, non_blocking=True) for t in pin)
-    dq, dk, dv = (t.to(dev, non_blocking=True) for t in din)
-    pout = torch.empty_like(pq)
-    dout = torch.empty_like(dq)
-    ws = torch.empty(apex.decode_workspace_bytes(wd.B, wd.H_q, wd.H_kv, wd.S_k, wd.d_h), dtype=torch.uint8,
-                     device=dev)
-    apex.apex_attn_rope_reserve(max(wp.S_k, wd.S_k), 128, 10000.0)
-    pout_h = torch.empty(pout.shape, dtype=pout.dtype, pin_memory=True)
-    dout_h = torch.empty(dout.shape, dtype=dout.dtype, pin_memory=True)
     stream = torch.cuda.current_stream()
+
+    pin = din = ()
+    if do_pre:
+        pin = inp.workload_inputs(wp, pin=True)
+        pq, pk, pv = (t.to(dev, non_blocking=True) for t in pin)
+        pout = torch.empty_like(pq)
+        pout_h = torch.empty(pout.shape, dtype=pout.dtype, pin_memory=True)
+        apex.apex_attn_rope_reserve(wp.S_k, wp.d_h, wp.rope_base)
+    if do_dec:
+        din = inp.workload_inputs(dataclasses.replace(wd, S_q=1), pin=True)
+        dq, dk, dv = (t.to(dev, non_blocking=True) for t in din)
+        dout = torch.empty_like(dq)
+        dout_h = torch.empty(dout.shape, dtype=dout.dtype, pin_memory=True)
+        ws = torch.empty(apex.decode_workspace_bytes(wd.B, wd.H_q, wd.H_kv, wd.S_k, wd.d_h), dtype=torch.uint8,
+                         device=dev)
+        apex.apex_attn_rope_reserve(wd.S_k, wd.d_h, wd.rope_base)
     torch.cuda.synchronize()
 
-    def step():
-        apex.fwd(pq, pk, pv, window=wp.window, q_pos0=wp.q_pos0, out=pout)
-        apex.decode(dq, dk, dv, wd.q_pos0, window=wd.window, out=dout, workspace=ws)
+    def prefill():
+        apex.fwd(pq, pk, pv, window=wp.window, q_pos0=wp.q_pos0, rope_base=wp.rope_base, out=pout)
 
-    for _ in range(max(3, args.warmup)):
-        step()
+    def decode():
+        apex.decode(dq, dk, dv, wd.q_pos0, window=wd.window, rope_base=wd.rope_base, out=dout, workspace=ws)
+
+    warm = max(3, args.warmup)
+    for _ in range(warm):
+        if do_pre:
+            prefill()
+        if do_dec:
+            decode()
     torch.cuda.synchronize()
     st = apex.apex_attn_device_status()
     if st != 0:
         raise RuntimeError("device status %d after warm-up" % st)
 
-    # ---- device-resident timed region
+    # ---- device-resident timed region: events before, between and after the two calls
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     sampler = ClockSampler(bus_id_of(local))
@@ -297,9 +309,11 @@ def run_ours(args):
     t_wall = time.perf_counter()
     for i in range(K):
         ev[i][0].record(stream)
-        apex.fwd(pq, pk, pv, window=wp.window, q_pos0=wp.q_pos0, out=pout)
+        if do_pre:
+            prefill()
         ev[i][1].record(stream)
-        apex.decode(dq, dk, dv, wd.q_pos0, window=wd.window, out=dout, workspace=ws)
+        if do_dec:
+            decode()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
@@ -313,22 +327,24 @@ def run_ours(args):
 
     # ---- end to end through the C ABI with pinned host buffers
     h2d = sum(t.numel() * t.element_size() for t in (*pin, *din))
-    d2h = pout.numel() * pout.element_size() + dout.numel() * dout.element_size()
+    d2h = (pout.numel() * 2 if do_pre else 0) + (dout.numel() * 2 if do_dec else 0)
     evx = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
     for i in range(K):
         evx[i][0].record(stream)
-        for dst, src in zip((pq, pk, pv), pin):
-            dst.copy_(src, non_blocking=True)
-        apex.fwd(pq, pk, pv, window=wp.window, q_pos0=wp.q_pos0, out=pout)
-        pout_h.copy_(pout, non_blocking=True)
+        if do_pre:
+            for dst, src in zip((pq, pk, pv), pin):
+                dst.copy_(src, non_blocking=True)
+            prefill()
+            pout_h.copy_(pout, non_blocking=True)
         evx[i][1].record(stream)
-        for dst, src in zip((dq, dk, dv), din):
-            dst.copy_(src, non_blocking=True)
-        apex.decode(dq, dk, dv, wd.q_pos0, window=wd.window, out=dout, workspace=ws)
-        dout_h.copy_(dout, non_blocking=True)
+        if do_dec:
+            for dst, src in zip((dq, dk, dv), din):
+                dst.copy_(src, non_blocking=True)
+            decode()
+            dout_h.copy_(dout, non_blocking=True)
         evx[i][2].record(stream)
     torch.cuda.synchronize()
     te_pre = sum(e[0].elapsed_time(e[1]) for e in evx) / 1e3
@@ -342,60 +358,65 @@ def run_ours(args):
     t_pre, t_dec, t_all, te_pre, te_dec = times.tolist()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and do_pre and do_dec:
         cpu = cpu_baseline(pin, din)
 
     if rank == 0:
         peaks = load_peaks()
-        pre_tflops = world * K * flops / t_pre / 1e12
-        dec_gbs = world * K * kvb / t_dec / 1e9
-        # per-launch figures of the kernels (one rank's launches)
-        pre_launch_s = t_pre / K
-        dec_launch_s = t_dec / K
-        dec_achieved = kvb / dec_launch_s / 1e9
-        pre_achieved = flops / pre_launch_s / 1e12
         traffic = load_traffic()
-        line = {
-            "metric": METRIC,
-            "value": pre_tflops,
-            "unit": "TFLOP/s",
-            "n_gpus": world,
-            "steps": K,
-            "warmup": max(3, args.warmup),
-            "ms_per_step": t_all * 1e3 / K,
-            "higher_is_better": True,
-            "scaling": "weak",
-            "vs_baseline": None,
-            "dtype": "bf16",
-            "data": "synthetic",
-            "config": {
-                "workload": "prefill %s (B4 Hq32 Hkv8 S4096 d128 W1024) + decode %s (B64 Hq32 Hkv8 Sk32768 "
-                            "d128 q_pos 32767)" % (PREFILL, DECODE),
-                "prefill_tflop_per_call": flops / 1e12,
-                "decode_kv_bytes_per_call": kvb,
-                "l2": "inputs larger than L2: prefill Q+K+V 201 MB, decode K+V 8.6 GB streamed between prefills",
-                "parallelism": "replica per GPU (independent problems)" if world > 1 else "1 GPU",
-            },
-            "decode": {"value": dec_gbs, "unit": "GB/s", "ms_per_call": dec_launch_s * 1e3,
-                       "frac_of_hbm": dec_achieved / peaks["hbm_gbs"]},
-            "prefill": {"value": pre_tflops, "unit": "TFLOP/s", "ms_per_call": pre_launch_s * 1e3,
-                        "frac_of_bf16": pre_achieved / peaks["bf16_tflops"],
-                        "frac_of_bf16_sustained": pre_achieved / peaks["bf16_tflops_sustained"]},
-            "roofline": {"kernel": "decode_split_kernel (+ its combine kernel, timed together)",
-                         "bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": dec_achieved / peaks["hbm_gbs"], "traffic": traffic.get("decode"),
-                         "peak_source": peaks["source"]},
-            "roofline_prefill": {"kernel": "prefill_kernel", "bound": "tensor", "achieved": pre_achieved,
-                                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                                 "frac": pre_achieved / peaks["bf16_tflops"], "traffic": traffic.get("prefill"),
-                                 "peak_source": peaks["source"] + " (burst)"},
-            "e2e": {"value": world * K * flops / te_pre / 1e12, "unit": "TFLOP/s",
-                    "decode_value": world * K * kvb / te_dec / 1e9, "decode_unit": "GB/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * K,
-            "clocks": clocks,
-            "wall_s_timed": t_wall,
+        line = {"metric": METRIC, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": warm,
+                "ms_per_step": t_all * 1e3 / K, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
+        desc = []
+        if do_pre:
+            desc.append("prefill %s (B%d Hq%d Hkv%d S%d d%d W%d)" % (wp.name, wp.B, wp.H_q, wp.H_kv, wp.S_q,
+                                                                     wp.d_h, wp.window))
+        if do_dec:
+            desc.append("decode (B%d Hq%d Hkv%d Sk%d d%d q_pos %d)" % (wd.B, wd.H_q, wd.H_kv, wd.S_k, wd.d_h,
+                                                                        wd.q_pos0))
+        line["config"] = {
+            "workload": " + ".join(desc),
+            "l2": "inputs larger than L2 (prefill Q+K+V >= 201 MB; decode K+V 8.6 GB streamed every step)",
+            "parallelism": "replica per GPU (independent problems)" if world > 1 else "1 GPU",
         }
+        e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        if do_pre:
+            pre_launch_s = t_pre / K
+            pre_achieved = flops / pre_launch_s / 1e12
+            line["value"] = world * K * flops / t_pre / 1e12
+            line["config"]["prefill_tflop_per_call"] = flops / 1e12
+            line["prefill"] = {"value": line["value"], "unit": "TFLOP/s", "ms_per_call": pre_launch_s * 1e3,
+                               "frac_of_bf16": pre_achieved / peaks["bf16_tflops"],
+                               "frac_of_bf16_sustained": pre_achieved / peaks["bf16_tflops_sustained"]}
+            line["roofline_prefill"] = {"kernel": "prefill_kernel", "bound": "tensor", "achieved": pre_achieved,
+                                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                        "frac": pre_achieved / peaks["bf16_tflops"],
+                                        "traffic": traffic.get("prefill_" + wp.name),
+                                        "peak_source": peaks["source"] + " (burst)"}
+            e2e.update({"value": world * K * flops / te_pre / 1e12, "unit": "TFLOP/s"})
+        if do_dec:
+            dec_launch_s = t_dec / K
+            dec_achieved = kvb / dec_launch_s / 1e9
+            line["config"]["decode_kv_bytes_per_call"] = kvb
+            line["decode"] = {"value": world * K * kvb / t_dec / 1e9, "unit": "GB/s",
+                              "ms_per_call": dec_launch_s * 1e3, "frac_of_hbm": dec_achieved / peaks["hbm_gbs"]}
+            line["roofline_decode"] = {"kernel": "decode_split_kernel (+ its combine kernel, timed together)",
+                                       "bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"],
+                                       "unit": "GB/s", "frac": dec_achieved / peaks["hbm_gbs"],
+                                       "traffic": traffic.get("decode"), "peak_source": peaks["source"]}
+            e2e.update({"decode_value": world * K * kvb / te_dec / 1e9, "decode_unit": "GB/s"})
+            if not do_pre:
+                line["value"], line["unit"] = line["decode"]["value"], "GB/s"
+                e2e.update({"value": e2e["decode_value"], "unit": "GB/s"})
+        # the kernel that dominates the step's time carries the roofline key
+        if do_dec and (not do_pre or t_dec >= t_pre):
+            line["roofline"] = line["roofline_decode"]
+        else:
+            line["roofline"] = line["roofline_prefill"]
+        line["e2e"] = e2e
+        line["gpu_launches"] = K * ((1 if do_pre else 0) + (2 if do_dec else 0))
+        line["clocks"] = clocks
+        line["wall_s_timed"] = t_wall
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line))
@@ -425,6 +446,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--part", choices=["all", "prefill", "decode"], default="all",
+                    help="run only one of the two calls per step (profiling)")
+    ap.add_argument("--prefill-workload", choices=["tiny", "gqa", "wide", "long"], default=PREFILL)
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -28,7 +28,17 @@
 namespace apex {
 namespace {
 
-constexpr int kThreads = 14 * 32;
+constexpr int kThreads = 16 * 32;
+// Register split (setmaxnreg): the block is launched with kLaunchRegs per
+// thread (512 x 128 = 65536); the softmax warpgroups take kRegsSoftmax, the
+// RoPE warpgroup kRegsRope and the producer/MMA warpgroup kRegsCtl.  The host
+// refuses to launch unless 128 x (2 kRegsSoftmax + kRegsRope + kRegsCtl) fits
+// in what the block was actually launched with.
+constexpr int kLaunchRegs = 128;
+constexpr int kRegsSoftmax = 168;
+constexpr int kRegsRope = 88;
+constexpr int kRegsCtl = 88;
+static_assert(128 * (2 * kRegsSoftmax + kRegsRope + kRegsCtl) <= kThreads * kLaunchRegs, "register split");
 constexpr int kWarpRope = 8;
 constexpr int kWarpTma = 12;
 constexpr int kWarpMma = 13;
@@ -46,8 +56,8 @@ struct Cfg {
     static constexpr int kBarOff = kVOff + kVStages * kTile;
     // barrier slots
     static constexpr int kBarQFull = 0;                       // [2]
-    static constexpr int kBarQReady = 2;                      // [1]
-    static constexpr int kBarKFull = 3;                       // [kKStages]
+    static constexpr int kBarQReady = 2;                      // [2]
+    static constexpr int kBarKFull = 4;                       // [kKStages]
     static constexpr int kBarKReady = kBarKFull + kKStages;   // [kKStages]
     static constexpr int kBarKEmpty = kBarKReady + kKStages;  // [kKStages]
     static constexpr int kBarVFull = kBarKEmpty + kKStages;   // [kVStages]
@@ -68,30 +78,125 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Rotate rows [0, 128) of a 128 x D tile stored as D/64 swizzled boxes.
-// Thread rt (0..127) takes 16-byte chunk (rt & 7) of rows (rt >> 3) + 16 k.
-// pos_of(row) returns the position of a row, or -1 to leave the row as is.
-template <int D, typename PosFn>
-__device__ __forceinline__ void rope_tile(uint8_t *tile, int rt, const float2 *cs_table, PosFn pos_of)
+// ---------------------------------------------------------------- RoPE in shared memory
+// Tiles are 128 rows x D bf16 stored as D/64 boxes of [128 rows][64 dims] with
+// the 128-byte swizzle of the TMA load.  A 16-byte chunk holds 4 interleaved
+// pairs (Part 1, §4.2): chunk c of box bx holds pairs 32 bx + 4 c + e, e < 4.
+
+// Rotate the 4 pairs of one chunk, (x_2i, x_2i+1) -> (x c - y s, x s + y c),
+// with the angles' (cos, sin) as packed pairs: C[h] = (c_{2h}, c_{2h+1}), etc.
+__device__ __forceinline__ uint4 rope_chunk(uint4 v, const uint64_t (&C)[2], const uint64_t (&S)[2])
 {
-    const int c = rt & 7;
-#pragma unroll 2
-    for (int k = 0; k < 8; ++k) {
-        const int row = (rt >> 3) + 16 * k;
-        const int pos = pos_of(row);
-        if (pos < 0) continue;
-        const float2 *cs_row = cs_table + (size_t)pos * (D / 2);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int bx = 0; bx < D / 64; ++bx) {
-            uint4 *ptr = reinterpret_cast<uint4 *>(tile + bx * kBoxBytes + swz128(row, c));
-            uint4 v = *ptr;
-            const float4 *cs4 = reinterpret_cast<const float4 *>(cs_row + bx * 32 + 4 * c);
-            const float4 a = __ldg(cs4), b = __ldg(cs4 + 1);
-            v.x = rope_pair_bf16(v.x, a.x, a.y);
-            v.y = rope_pair_bf16(v.y, a.z, a.w);
-            v.z = rope_pair_bf16(v.z, b.x, b.y);
-            v.w = rope_pair_bf16(v.w, b.z, b.w);
-            *ptr = v;
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t w0 = w[2 * h], w1 = w[2 * h + 1];
+        const uint64_t X = f2_pack(bf16lo_to_f32(w0), bf16lo_to_f32(w1));  // even elements
+        const uint64_t Y = f2_pack(bf16hi_to_f32(w0), bf16hi_to_f32(w1));  // odd elements
+        const uint64_t Xn = f2_fma(Y, f2_neg(S[h]), f2_mul(X, C[h]));
+        const uint64_t Yn = f2_fma(X, S[h], f2_mul(Y, C[h]));
+        float x0, x1, y0, y1;
+        f2_unpack(Xn, x0, x1);
+        f2_unpack(Yn, y0, y1);
+        w[2 * h] = pack_bf16x2(x0, y0);
+        w[2 * h + 1] = pack_bf16x2(x1, y1);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// K tile, key row r at position key0 + r.  Thread rt owns chunk c = rt & 7 of
+// rows r0 + 16 k (r0 = rt >> 3, k < 8) in every box.  The angles of successive
+// rows advance by 16 positions, so (cos, sin) follow the recurrence
+// z_{k+1} = z_k * w with w = (cos 16 theta, sin 16 theta), seeded once per tile
+// from the table at position key0 + r0.
+template <int D>
+struct KRope {
+    static constexpr int NB = D / 64;
+    uint64_t WC[NB][2], WS[NB][2];  // step rotation per pair
+    float4 seed[NB][2];             // (c0, s0, c1, s1), (c2, s2, c3, s3) at the tile's first row
+
+    __device__ __forceinline__ void init(const float2 *table, int c)
+    {
+#pragma unroll
+        for (int bx = 0; bx < NB; ++bx) {
+            const float4 *p = reinterpret_cast<const float4 *>(table + 16 * (D / 2) + 32 * bx + 4 * c);
+            const float4 a = __ldg(p), b = __ldg(p + 1);
+            WC[bx][0] = f2_pack(a.x, a.z);
+            WS[bx][0] = f2_pack(a.y, a.w);
+            WC[bx][1] = f2_pack(b.x, b.z);
+            WS[bx][1] = f2_pack(b.y, b.w);
+        }
+    }
+    __device__ __forceinline__ void load_seed(const float2 *table, int pos, int c)
+    {
+#pragma unroll
+        for (int bx = 0; bx < NB; ++bx) {
+            const float4 *p = reinterpret_cast<const float4 *>(table + (size_t)pos * (D / 2) + 32 * bx + 4 * c);
+            seed[bx][0] = __ldg(p);
+            seed[bx][1] = __ldg(p + 1);
+        }
+    }
+    // rotate the tile; reads the seed (the caller may then load the next one)
+    __device__ __forceinline__ void rotate(uint8_t *tile, int rt)
+    {
+        const int c = rt & 7, r0 = rt >> 3;
+        uint64_t C[NB][2], S[NB][2];
+#pragma unroll
+        for (int bx = 0; bx < NB; ++bx) {
+            C[bx][0] = f2_pack(seed[bx][0].x, seed[bx][0].z);
+            S[bx][0] = f2_pack(seed[bx][0].y, seed[bx][0].w);
+            C[bx][1] = f2_pack(seed[bx][1].x, seed[bx][1].z);
+            S[bx][1] = f2_pack(seed[bx][1].y, seed[bx][1].w);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int row = r0 + 16 * k;
+#pragma unroll
+            for (int bx = 0; bx < NB; ++bx) {
+                uint4 *ptr = reinterpret_cast<uint4 *>(tile + bx * kBoxBytes + swz128(row, c));
+                *ptr = rope_chunk(*ptr, C[bx], S[bx]);
+                if (k < 7) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t Cn = f2_fma(C[bx][h], WC[bx][h], f2_mul(S[bx][h], f2_neg(WS[bx][h])));
+                        const uint64_t Sn = f2_fma(C[bx][h], WS[bx][h], f2_mul(S[bx][h], WC[bx][h]));
+                        C[bx][h] = Cn;
+                        S[bx][h] = Sn;
+                    }
+                }
+            }
+        }
+    }
+};
+
+// Q tile: rows are head-major (row = head * P + p), so all G heads of one
+// position p share one set of angles.  Thread rt takes the (p, chunk) combos
+// rt, rt + 128, ... and rotates that chunk of the G rows of position p.
+template <int D>
+__device__ __forceinline__ void rope_q_tile(uint8_t *tile, int rt, const float2 *table, int pos0, int G, int P,
+                                            int valid_p)
+{
+    constexpr int NB = D / 64;
+    for (int q = rt; q < P * 8; q += 128) {
+        const int p = q >> 3, c = q & 7;
+        if (p >= valid_p) continue;
+        uint64_t C[NB][2], S[NB][2];
+#pragma unroll
+        for (int bx = 0; bx < NB; ++bx) {
+            const float4 *t = reinterpret_cast<const float4 *>(table + (size_t)(pos0 + p) * (D / 2) + 32 * bx + 4 * c);
+            const float4 a = __ldg(t), b = __ldg(t + 1);
+            C[bx][0] = f2_pack(a.x, a.z);
+            S[bx][0] = f2_pack(a.y, a.w);
+            C[bx][1] = f2_pack(b.x, b.z);
+            S[bx][1] = f2_pack(b.y, b.w);
+        }
+        for (int hl = 0; hl < G; ++hl) {
+            const int row = hl * P + p;
+#pragma unroll
+            for (int bx = 0; bx < NB; ++bx) {
+                uint4 *ptr = reinterpret_cast<uint4 *>(tile + bx * kBoxBytes + swz128(row, c));
+                *ptr = rope_chunk(*ptr, C[bx], S[bx]);
+            }
         }
     }
 }
@@ -126,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(C::kBarQFull + 0), 1);
         mbar_init(bar(C::kBarQFull + 1), 1);
-        mbar_init(bar(C::kBarQReady), 4);
+        mbar_init(bar(C::kBarQReady + 0), 4);
+        mbar_init(bar(C::kBarQReady + 1), 4);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(bar(C::kBarKFull + s), 1);
             mbar_init(bar(C::kBarKReady + s), 4);
@@ -149,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::kTmemSlot);
 
+    if (warp >= kWarpTma) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -202,23 +309,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 8 * s,
                             smem_desc_sw128(vb + s * 2048, kBoxBytes, 1024), idesc_pv, (acc || s > 0) ? 1u : 0u);
             };
-            mbar_wait(bar(C::kBarQReady), 0, p.wait);
             mbar_wait(bar(C::kBarKReady + 0), 0, p.wait);
+            mbar_wait(bar(C::kBarQReady + 0), 0, p.wait);
             tc_fence_after();
             issue_qk(0, 0);
             tc_commit(bar(C::kBarSFull + 0));
+            mbar_wait(bar(C::kBarQReady + 1), 0, p.wait);
+            tc_fence_after();
             issue_qk(1, 0);
             tc_commit(bar(C::kBarSFull + 1));
             tc_commit(bar(C::kBarKEmpty + 0));
             for (int j = 0; j < n_kt; ++j) {
                 const bool nxt = j + 1 < n_kt;
                 const int ks = (j + 1) % kKStages, vs = j % kVStages;
-                if (nxt) mbar_wait(bar(C::kBarKReady + ks), ((j + 1) / kKStages) & 1, p.wait);
                 mbar_wait(bar(C::kBarVFull + vs), (j / kVStages) & 1, p.wait);
                 mbar_wait(bar(C::kBarPReady + 0), j & 1, p.wait);
                 tc_fence_after();
                 issue_pv(0, vs, j > 0);
                 if (nxt) {
+                    mbar_wait(bar(C::kBarKReady + ks), ((j + 1) / kKStages) & 1, p.wait);
+                    tc_fence_after();
                     issue_qk(0, ks);
                     tc_commit(bar(C::kBarSFull + 0));
                 } else {
@@ -237,34 +347,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp >= kWarpRope) {
-        // ------------------------------------------------------------ RoPE warps
+    } else if (warp >= kWarpRope && warp < kWarpTma) {
+        // ------------------------------------------------------------ RoPE warps (K tiles)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRope));
         const int rt = threadIdx.x - kWarpRope * 32;
-        mbar_wait(bar(C::kBarQFull + 0), 0, p.wait);
-        mbar_wait(bar(C::kBarQFull + 1), 0, p.wait);
-        for (int t = 0; t < 2; ++t) {
-            rope_tile<D>(smem + C::kQOff + t * C::kTile, rt, p.rope.cs, [&](int row) {
-                const int r = r0 + t * P + row % P;
-                return r < p.S_q ? p.q_pos0 + r : -1;
-            });
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::kBarQReady));
+        const int c = rt & 7, r0 = rt >> 3;
+        const int max_row = p.rope.max_pos - 1;
+        KRope<D> kr;
+        kr.init(p.rope.cs, c);
+        kr.load_seed(p.rope.cs, min(128 * j_lo + r0, max_row), c);
         for (int j = 0; j < n_kt; ++j) {
             const int ks = j % kKStages;
-            const int key0 = 128 * (j_lo + j);
             mbar_wait(bar(C::kBarKFull + ks), (j / kKStages) & 1, p.wait);
-            rope_tile<D>(smem + C::kKOff + ks * C::kTile, rt, p.rope.cs, [&](int row) {
-                const int key = key0 + row;
-                return key < p.S_k ? key : -1;
-            });
+            kr.rotate(smem + C::kKOff + ks * C::kTile, rt);
+            if (j + 1 < n_kt) kr.load_seed(p.rope.cs, min(128 * (j_lo + j + 1) + r0, max_row), c);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarKReady + ks));
         }
-    } else {
+    } else if (warp < kWarpRope) {
         // ------------------------------------------------------------ softmax + epilogue
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         const int t = warp >> 2;
         const int i = (warp & 3) * 32 + lane;  // row of the M tile == TMEM lane
         const int r = r0 + t * P + i % P;      // query row index
@@ -275,6 +378,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t o_addr = lane_base + C::col_o(t);
         float m_run = -INFINITY, l_run = 0.f;
 
+        // RoPE of this warpgroup's Q tile (rows of position index >= valid are padding)
+        mbar_wait(bar(C::kBarQFull + t), 0, p.wait);
+        rope_q_tile<D>(smem + C::kQOff + t * C::kTile, i, p.rope.cs, p.q_pos0 + r0 + t * P, p.G, P,
+                       min(P, p.S_q - (r0 + t * P)));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kBarQReady + t));
+
         for (int j = 0; j < n_kt; ++j) {
             mbar_wait(bar(C::kBarSFull + t), j & 1, p.wait);
             tc_fence_after();
@@ -282,25 +393,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool full_vis = (kstart + 127 <= m) && (W == 0 || m - kstart < W);
             const bool all_full = __all_sync(0xffffffffu, full_vis);
 
-            // pass 1: row max of the visible scores
-            float mx = -INFINITY;
+            // columns [lo_c, hi_c] of this tile are visible to the row (Part 2, §10.2)
+            const int hi_c = m - kstart;
+            const int lo_c = (W > 0) ? m - W + 1 - kstart : -1000000;
+
+            // the whole 128-column row of S in registers
+            uint32_t v[128];
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t v[32];
-                tmem_ld32(s_addr + 32 * ch, v);
-                tmem_wait_ld();
-                if (all_full) {
+            for (int ch = 0; ch < 4; ++ch)
+                tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * ch]));
+            tmem_wait_ld();
+            if (!all_full) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int key = kstart + 32 * ch + e;
-                        const bool vis = key <= m && (W == 0 || m - key < W);
-                        if (vis) mx = fmaxf(mx, __uint_as_float(v[e]));
-                    }
-                }
+                for (int e = 0; e < 128; ++e)
+                    if (e < lo_c || e > hi_c) v[e] = __float_as_uint(-INFINITY);
             }
+            // row max of the visible scores (8 independent chains)
+            float acc[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) acc[a] = __uint_as_float(v[a]);
+#pragma unroll
+            for (int e = 8; e < 128; e += 16)
+#pragma unroll
+                for (int a = 0; a < 8; ++a)
+                    acc[a] = fmax3(acc[a], __uint_as_float(v[e + a]), __uint_as_float(v[e + 8 + a]));
+            const float mx = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
             const float m_tile = mx * p.scale_log2;
             const float m_new = fmaxf(m_run, m_tile);
             const bool need = (m_run != -INFINITY) && (m_new > m_run + 8.f);
@@ -309,40 +426,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
                 l_run *= alpha;
                 m_run = m_new;
-#pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t v[32];
-                    tmem_ld32(o_addr + 32 * ch, v);
+#pragma unroll 1
+                for (int ch = 0; ch < D / 16; ++ch) {
+                    uint32_t o[16];
+                    tmem_ld16(o_addr + 16 * ch, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(o_addr + 32 * ch, v);
+                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st16(o_addr + 16 * ch, o);
                 }
             } else if (m_run == -INFINITY) {
                 m_run = m_new;
             }
             const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
 
-            // pass 2: p = exp2(s * log2(e)/sqrt(d) - m), row sum, P -> TMEM as bf16
+            // p = exp2(s * log2(e)/sqrt(d) - m), row sum, P -> TMEM as bf16 over S
+            const uint64_t SC = f2_pack(p.scale_log2, p.scale_log2);
+            const uint64_t NM = f2_pack(-m_use, -m_use);
+            uint64_t lacc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t v[32];
-                tmem_ld32(s_addr + 32 * ch, v);
-                tmem_wait_ld();
+            for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e2 = 0; e2 < 16; ++e2) {
-                    float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e2]), p.scale_log2, -m_use));
-                    float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e2 + 1]), p.scale_log2, -m_use));
-                    if (!all_full) {
-                        const int key = kstart + 32 * ch + 2 * e2;
-                        if (!(key <= m && (W == 0 || m - key < W))) p0 = 0.f;
-                        if (!(key + 1 <= m && (W == 0 || m - key - 1 < W))) p1 = 0.f;
-                    }
-                    l_run += p0 + p1;
+                    const uint64_t x = f2_pack(__uint_as_float(v[32 * q4 + 2 * e2]), __uint_as_float(v[32 * q4 + 2 * e2 + 1]));
+                    float y0, y1;
+                    f2_unpack(f2_fma(x, SC, NM), y0, y1);
+                    const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+                    lacc[e2 & 3] = f2_add(lacc[e2 & 3], f2_pack(p0, p1));
                     pk[e2] = pack_bf16x2(p0, p1);
                 }
-                tmem_st16(s_addr + 16 * ch, pk);
+                tmem_st16(s_addr + 16 * q4, pk);
+            }
+            {
+                float a0, a1;
+                f2_unpack(f2_add(f2_add(lacc[0], lacc[1]), f2_add(lacc[2], lacc[3])), a0, a1);
+                l_run += a0 + a1;
             }
             tmem_wait_st();
             tc_fence_before();
@@ -397,6 +516,12 @@ cudaError_t launch_t(const PrefillLaunch &L, cudaStream_t stream)
     cudaError_t err =
         cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
+    // setmaxnreg.inc blocks until the block's own pool can serve it: never
+    // launch unless the split fits the registers the block is launched with
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
+    if (err != cudaSuccess) return err;
+    if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
     prefill_kernel<D><<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_o, L.p);
     return cudaGetLastError();
 }

@@ -344,10 +344,10 @@ apex_status apex_attn_fwd(const void *q, const void *k, const void *v, void *out
     PrefillLaunch L;
     memset(&L, 0, sizeof L);
     if (!make_map(&L.tm_q, q, d_h, S_q, B * H_q, rows_per_head, G) ||
-        !make_map(&L.tm_o, out, d_h, S_q, B * H_q, rows_per_head, G) ||
         !make_map(&L.tm_k, k, d_h, S_k, B * H_kv, 128, 1) || !make_map(&L.tm_v, v, d_h, S_k, B * H_kv, 128, 1))
         return APEX_ERR_CUDA;
     PrefillParams &p = L.p;
+    p.out = static_cast<uint16_t *>(out);
     p.rope = tv;
     p.wait = WaitCtl{st->status, wait_timeout_ns()};
     p.B = B;
@@ -363,7 +363,7 @@ apex_status apex_attn_fwd(const void *q, const void *k, const void *v, void *out
     p.n_qblocks = (S_q + 2 * rows_per_head - 1) / (2 * rows_per_head);
     p.n_work = B * H_kv * p.n_qblocks;
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d_h));
-    L.grid = p.n_work;
+    L.grid = std::min(p.n_work, st->sm_count);
     if (launch_prefill(L, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return APEX_ERR_CUDA;
     return APEX_OK;
 }

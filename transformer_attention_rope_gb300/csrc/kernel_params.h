@@ -56,6 +56,7 @@ int decode_ctas_per_sm(int d_h, int G);
 
 // ----------------------------------------------------------------- prefill
 struct PrefillParams {
+    uint16_t *out;  // [B, H_q, S_q, d_h] bf16
     RopeTableView rope;
     WaitCtl wait;
     int B, H_q, H_kv, G, S_q, S_k, d_h;
@@ -63,14 +64,14 @@ struct PrefillParams {
     int q_pos0;
     int rows_per_head;   // query positions per head in one 128-row M tile (128 / G)
     int n_qblocks;       // position blocks per (b, kv-head); a block = 2 M tiles
-    int n_work;          // B * H_kv * n_qblocks
+    int n_work;          // B * H_kv * n_qblocks (work items, walked by a persistent grid)
     float scale_log2;    // log2(e) / sqrt(d_h)
 };
 
 struct PrefillLaunch {
-    CUtensorMap tm_q, tm_k, tm_v, tm_o;
+    CUtensorMap tm_q, tm_k, tm_v;
     PrefillParams p;
-    int grid;
+    int grid;  // persistent CTAs (at most one per SM)
 };
 
 cudaError_t launch_prefill(const PrefillLaunch &L, cudaStream_t stream);

@@ -57,7 +57,8 @@ struct Cfg {
     // barrier slots
     static constexpr int kBarQFull = 0;                       // [2]
     static constexpr int kBarQReady = 2;                      // [2]
-    static constexpr int kBarKFull = 4;                       // [kKStages]
+    static constexpr int kBarQEmpty = 4;                      // [2]
+    static constexpr int kBarKFull = 6;                       // [kKStages]
     static constexpr int kBarKReady = kBarKFull + kKStages;   // [kKStages]
     static constexpr int kBarKEmpty = kBarKReady + kKStages;  // [kKStages]
     static constexpr int kBarVFull = kBarKEmpty + kKStages;   // [kVStages]
@@ -201,11 +202,41 @@ __device__ __forceinline__ void rope_q_tile(uint8_t *tile, int rt, const float2 
     }
 }
 
+// One work item: (batch, kv head) unit and a block of 2P query rows.
+struct Item {
+    int unit, b, hk, r0, j_lo, n_kt, zq;
+};
+
+__device__ __forceinline__ Item make_item(const PrefillParams &p, int w)
+{
+    Item it;
+    const int units = p.B * p.H_kv;
+    const int qblock = p.n_qblocks - 1 - w / units;  // latest positions (most key tiles) first
+    it.unit = w % units;
+    it.b = it.unit / p.H_kv;
+    it.hk = it.unit % p.H_kv;
+    const int P = p.rows_per_head;
+    it.r0 = qblock * 2 * P;
+    const int rows = min(2 * P, p.S_q - it.r0);
+    const int m_first = p.q_pos0 + it.r0, m_last = p.q_pos0 + it.r0 + rows - 1;
+    it.j_lo = (p.window > 0) ? max(0, m_first - p.window + 1) / 128 : 0;
+    it.n_kt = m_last / 128 - it.j_lo + 1;
+    it.zq = it.b * p.H_q + it.hk * p.G;
+    return it;
+}
+
+// k-th item of this CTA: rounds of gridDim.x items, walked in alternating
+// direction so that the heavy items of each round spread over the CTAs.
+__device__ __forceinline__ int item_index(int k)
+{
+    const int g = gridDim.x, c = blockIdx.x;
+    return k * g + ((k & 1) ? (g - 1 - c) : c);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                   const PrefillParams p)
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p)
 {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -213,26 +244,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto bar = [&](int i) -> uint32_t { return sb + C::kBarOff + 8 * i; };
-
-    // ---- work item, heaviest (latest positions) first
-    const int units = p.B * p.H_kv;
-    const int qblock = p.n_qblocks - 1 - (int)blockIdx.x / units;
-    const int unit = (int)blockIdx.x % units;
-    const int b = unit / p.H_kv, hk = unit % p.H_kv;
     const int P = p.rows_per_head;
-    const int r0 = qblock * 2 * P;
-    const int rows_in_block = min(2 * P, p.S_q - r0);
-    const int m_first = p.q_pos0 + r0;
-    const int m_last = p.q_pos0 + r0 + rows_in_block - 1;
-    const int j_lo = (p.window > 0) ? max(0, m_first - p.window + 1) / 128 : 0;
-    const int n_kt = m_last / 128 - j_lo + 1;
-    const int zq = b * p.H_q + hk * p.G;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(C::kBarQFull + 0), 1);
-        mbar_init(bar(C::kBarQFull + 1), 1);
-        mbar_init(bar(C::kBarQReady + 0), 4);
-        mbar_init(bar(C::kBarQReady + 1), 4);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(C::kBarQFull + t), 1);
+            mbar_init(bar(C::kBarQReady + t), 4);
+            mbar_init(bar(C::kBarQEmpty + t), 1);
+            mbar_init(bar(C::kBarSFull + t), 1);
+            mbar_init(bar(C::kBarPReady + t), 4);
+            mbar_init(bar(C::kBarODone + t), 1);
+        }
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(bar(C::kBarKFull + s), 1);
             mbar_init(bar(C::kBarKReady + s), 4);
@@ -241,11 +263,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(bar(C::kBarVFull + s), 1);
             mbar_init(bar(C::kBarVEmpty + s), 1);
-        }
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(bar(C::kBarSFull + t), 1);
-            mbar_init(bar(C::kBarPReady + t), 4);
-            mbar_init(bar(C::kBarODone + t), 1);
         }
         fence_mbarrier_init();
     }
@@ -262,29 +279,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            tma_prefetch_desc(&tm_o);
-            for (int t = 0; t < 2; ++t) {
-                mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTile);
+            int kc = 0;  // K/V tiles issued so far (ring position)
+            for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
+                const Item it = make_item(p, w);
+                for (int t = 0; t < 2; ++t) {
+                    mbar_wait(bar(C::kBarQEmpty + t), (k & 1) ^ 1, p.wait);
+                    mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTile);
 #pragma unroll
-                for (int bx = 0; bx < C::kBoxes; ++bx)
-                    tma_load_3d(sb + C::kQOff + t * C::kTile + bx * kBoxBytes, &tm_q, bar(C::kBarQFull + t),
-                                64 * bx, r0 + t * P, zq);
-            }
-            for (int j = 0; j < n_kt; ++j) {
-                const int key0 = 128 * (j_lo + j);
-                const int ks = j % kKStages, vs = j % kVStages;
-                mbar_wait(bar(C::kBarKEmpty + ks), ((j / kKStages) & 1) ^ 1, p.wait);
-                mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTile);
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                        tma_load_3d(sb + C::kQOff + t * C::kTile + bx * kBoxBytes, &tm_q, bar(C::kBarQFull + t),
+                                    64 * bx, it.r0 + t * P, it.zq);
+                }
+                for (int j = 0; j < it.n_kt; ++j, ++kc) {
+                    const int key0 = 128 * (it.j_lo + j);
+                    const int ks = kc % kKStages, vs = kc % kVStages;
+                    mbar_wait(bar(C::kBarKEmpty + ks), ((kc / kKStages) & 1) ^ 1, p.wait);
+                    mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTile);
 #pragma unroll
-                for (int bx = 0; bx < C::kBoxes; ++bx)
-                    tma_load_3d(sb + C::kKOff + ks * C::kTile + bx * kBoxBytes, &tm_k, bar(C::kBarKFull + ks),
-                                64 * bx, key0, unit);
-                mbar_wait(bar(C::kBarVEmpty + vs), ((j / kVStages) & 1) ^ 1, p.wait);
-                mbar_arrive_expect_tx(bar(C::kBarVFull + vs), C::kTile);
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                        tma_load_3d(sb + C::kKOff + ks * C::kTile + bx * kBoxBytes, &tm_k, bar(C::kBarKFull + ks),
+                                    64 * bx, key0, it.unit);
+                    mbar_wait(bar(C::kBarVEmpty + vs), ((kc / kVStages) & 1) ^ 1, p.wait);
+                    mbar_arrive_expect_tx(bar(C::kBarVFull + vs), C::kTile);
 #pragma unroll
-                for (int bx = 0; bx < C::kBoxes; ++bx)
-                    tma_load_3d(sb + C::kVOff + vs * C::kTile + bx * kBoxBytes, &tm_v, bar(C::kBarVFull + vs),
-                                64 * bx, key0, unit);
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                        tma_load_3d(sb + C::kVOff + vs * C::kTile + bx * kBoxBytes, &tm_v, bar(C::kBarVFull + vs),
+                                    64 * bx, key0, it.unit);
+                }
             }
         }
     } else if (warp == kWarpMma) {
@@ -309,194 +330,212 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 8 * s,
                             smem_desc_sw128(vb + s * 2048, kBoxBytes, 1024), idesc_pv, (acc || s > 0) ? 1u : 0u);
             };
-            mbar_wait(bar(C::kBarKReady + 0), 0, p.wait);
-            mbar_wait(bar(C::kBarQReady + 0), 0, p.wait);
-            tc_fence_after();
-            issue_qk(0, 0);
-            tc_commit(bar(C::kBarSFull + 0));
-            mbar_wait(bar(C::kBarQReady + 1), 0, p.wait);
-            tc_fence_after();
-            issue_qk(1, 0);
-            tc_commit(bar(C::kBarSFull + 1));
-            tc_commit(bar(C::kBarKEmpty + 0));
-            for (int j = 0; j < n_kt; ++j) {
-                const bool nxt = j + 1 < n_kt;
-                const int ks = (j + 1) % kKStages, vs = j % kVStages;
-                mbar_wait(bar(C::kBarVFull + vs), (j / kVStages) & 1, p.wait);
-                mbar_wait(bar(C::kBarPReady + 0), j & 1, p.wait);
-                tc_fence_after();
-                issue_pv(0, vs, j > 0);
-                if (nxt) {
-                    mbar_wait(bar(C::kBarKReady + ks), ((j + 1) / kKStages) & 1, p.wait);
+            int kc = 0;
+            for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
+                const Item it = make_item(p, w);
+                const int n = it.n_kt;
+                mbar_wait(bar(C::kBarKReady + kc % kKStages), (kc / kKStages) & 1, p.wait);
+                for (int t = 0; t < 2; ++t) {
+                    mbar_wait(bar(C::kBarQReady + t), k & 1, p.wait);
                     tc_fence_after();
-                    issue_qk(0, ks);
-                    tc_commit(bar(C::kBarSFull + 0));
-                } else {
-                    tc_commit(bar(C::kBarODone + 0));
+                    issue_qk(t, kc % kKStages);
+                    tc_commit(bar(C::kBarSFull + t));
+                    if (n == 1) tc_commit(bar(C::kBarQEmpty + t));  // last read of Q_t
                 }
-                mbar_wait(bar(C::kBarPReady + 1), j & 1, p.wait);
-                tc_fence_after();
-                issue_pv(1, vs, j > 0);
-                tc_commit(bar(C::kBarVEmpty + vs));
-                if (nxt) {
-                    issue_qk(1, ks);
-                    tc_commit(bar(C::kBarSFull + 1));
-                    tc_commit(bar(C::kBarKEmpty + ks));
-                } else {
-                    tc_commit(bar(C::kBarODone + 1));
+                tc_commit(bar(C::kBarKEmpty + kc % kKStages));
+                for (int j = 0; j < n; ++j) {
+                    const int g = kc + j;
+                    const bool nxt = j + 1 < n;
+                    const bool last_qk = j + 2 == n;  // the next QK is this item's last read of Q
+                    const int ks = (g + 1) % kKStages, vs = g % kVStages;
+                    mbar_wait(bar(C::kBarVFull + vs), (g / kVStages) & 1, p.wait);
+                    mbar_wait(bar(C::kBarPReady + 0), g & 1, p.wait);
+                    tc_fence_after();
+                    issue_pv(0, vs, j > 0);
+                    if (nxt) {
+                        mbar_wait(bar(C::kBarKReady + ks), ((g + 1) / kKStages) & 1, p.wait);
+                        tc_fence_after();
+                        issue_qk(0, ks);
+                        tc_commit(bar(C::kBarSFull + 0));
+                        if (last_qk) tc_commit(bar(C::kBarQEmpty + 0));
+                    } else {
+                        tc_commit(bar(C::kBarODone + 0));
+                    }
+                    mbar_wait(bar(C::kBarPReady + 1), g & 1, p.wait);
+                    tc_fence_after();
+                    issue_pv(1, vs, j > 0);
+                    tc_commit(bar(C::kBarVEmpty + vs));
+                    if (nxt) {
+                        issue_qk(1, ks);
+                        tc_commit(bar(C::kBarSFull + 1));
+                        if (last_qk) tc_commit(bar(C::kBarQEmpty + 1));
+                        tc_commit(bar(C::kBarKEmpty + ks));
+                    } else {
+                        tc_commit(bar(C::kBarODone + 1));
+                    }
                 }
+                kc += n;
             }
         }
     } else if (warp >= kWarpRope && warp < kWarpTma) {
-        // ------------------------------------------------------------ RoPE warps (K tiles)
+        // ------------------------------------------------------------ RoPE warps
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRope));
         const int rt = threadIdx.x - kWarpRope * 32;
         const int c = rt & 7, r0 = rt >> 3;
         const int max_row = p.rope.max_pos - 1;
         KRope<D> kr;
         kr.init(p.rope.cs, c);
-        kr.load_seed(p.rope.cs, min(128 * j_lo + r0, max_row), c);
-        for (int j = 0; j < n_kt; ++j) {
-            const int ks = j % kKStages;
-            mbar_wait(bar(C::kBarKFull + ks), (j / kKStages) & 1, p.wait);
-            kr.rotate(smem + C::kKOff + ks * C::kTile, rt);
-            if (j + 1 < n_kt) kr.load_seed(p.rope.cs, min(128 * (j_lo + j + 1) + r0, max_row), c);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::kBarKReady + ks));
+        int kc = 0;
+        for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
+            const Item it = make_item(p, w);
+            kr.load_seed(p.rope.cs, min(128 * it.j_lo + r0, max_row), c);
+            for (int j = 0; j < it.n_kt; ++j, ++kc) {
+                const int ks = kc % kKStages;
+                mbar_wait(bar(C::kBarKFull + ks), (kc / kKStages) & 1, p.wait);
+                kr.rotate(smem + C::kKOff + ks * C::kTile, rt);
+                if (j + 1 < it.n_kt) kr.load_seed(p.rope.cs, min(128 * (it.j_lo + j + 1) + r0, max_row), c);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarKReady + ks));
+            }
         }
     } else if (warp < kWarpRope) {
         // ------------------------------------------------------------ softmax + epilogue
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         const int t = warp >> 2;
         const int i = (warp & 3) * 32 + lane;  // row of the M tile == TMEM lane
-        const int r = r0 + t * P + i % P;      // query row index
-        const int m = p.q_pos0 + r;            // its position
         const int W = p.window;
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t s_addr = lane_base + C::col_s(t);
         const uint32_t o_addr = lane_base + C::col_o(t);
-        float m_run = -INFINITY, l_run = 0.f;
-
-        // RoPE of this warpgroup's Q tile (rows of position index >= valid are padding)
-        mbar_wait(bar(C::kBarQFull + t), 0, p.wait);
-        rope_q_tile<D>(smem + C::kQOff + t * C::kTile, i, p.rope.cs, p.q_pos0 + r0 + t * P, p.G, P,
-                       min(P, p.S_q - (r0 + t * P)));
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::kBarQReady + t));
-
-        for (int j = 0; j < n_kt; ++j) {
-            mbar_wait(bar(C::kBarSFull + t), j & 1, p.wait);
-            tc_fence_after();
-            const int kstart = 128 * (j_lo + j);
-            const bool full_vis = (kstart + 127 <= m) && (W == 0 || m - kstart < W);
-            const bool all_full = __all_sync(0xffffffffu, full_vis);
-
-            // columns [lo_c, hi_c] of this tile are visible to the row (Part 2, §10.2)
-            const int hi_c = m - kstart;
-            const int lo_c = (W > 0) ? m - W + 1 - kstart : -1000000;
-
-            // the whole 128-column row of S in registers
-            uint32_t v[128];
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch)
-                tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * ch]));
-            tmem_wait_ld();
-            if (!all_full) {
-#pragma unroll
-                for (int e = 0; e < 128; ++e)
-                    if (e < lo_c || e > hi_c) v[e] = __float_as_uint(-INFINITY);
-            }
-            // row max of the visible scores (8 independent chains)
-            float acc[8];
-#pragma unroll
-            for (int a = 0; a < 8; ++a) acc[a] = __uint_as_float(v[a]);
-#pragma unroll
-            for (int e = 8; e < 128; e += 16)
-#pragma unroll
-                for (int a = 0; a < 8; ++a)
-                    acc[a] = fmax3(acc[a], __uint_as_float(v[e + a]), __uint_as_float(v[e + 8 + a]));
-            const float mx = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
-            const float m_tile = mx * p.scale_log2;
-            const float m_new = fmaxf(m_run, m_tile);
-            const bool need = (m_run != -INFINITY) && (m_new > m_run + 8.f);
-            if (__any_sync(0xffffffffu, need)) {
-                // raise the reference max of every row of this warp and rescale O and l
-                const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
-                l_run *= alpha;
-                m_run = m_new;
-#pragma unroll 1
-                for (int ch = 0; ch < D / 16; ++ch) {
-                    uint32_t o[16];
-                    tmem_ld16(o_addr + 16 * ch, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st16(o_addr + 16 * ch, o);
-                }
-            } else if (m_run == -INFINITY) {
-                m_run = m_new;
-            }
-            const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-
-            // p = exp2(s * log2(e)/sqrt(d) - m), row sum, P -> TMEM as bf16 over S
-            const uint64_t SC = f2_pack(p.scale_log2, p.scale_log2);
-            const uint64_t NM = f2_pack(-m_use, -m_use);
-            uint64_t lacc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e2 = 0; e2 < 16; ++e2) {
-                    const uint64_t x = f2_pack(__uint_as_float(v[32 * q4 + 2 * e2]), __uint_as_float(v[32 * q4 + 2 * e2 + 1]));
-                    float y0, y1;
-                    f2_unpack(f2_fma(x, SC, NM), y0, y1);
-                    const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
-                    lacc[e2 & 3] = f2_add(lacc[e2 & 3], f2_pack(p0, p1));
-                    pk[e2] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(s_addr + 16 * q4, pk);
-            }
-            {
-                float a0, a1;
-                f2_unpack(f2_add(f2_add(lacc[0], lacc[1]), f2_add(lacc[2], lacc[3])), a0, a1);
-                l_run += a0 + a1;
-            }
-            tmem_wait_st();
-            tc_fence_before();
+        // RoPE of this warpgroup's Q tile of an item (rows at or past S_q are padding)
+        auto rotate_q = [&](const Item &it, int k) {
+            mbar_wait(bar(C::kBarQFull + t), k & 1, p.wait);
+            rope_q_tile<D>(smem + C::kQOff + t * C::kTile, i, p.rope.cs, p.q_pos0 + it.r0 + t * P, p.G, P,
+                           min(P, p.S_q - (it.r0 + t * P)));
+            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::kBarPReady + t));
-        }
+            if (lane == 0) mbar_arrive(bar(C::kBarQReady + t));
+        };
+        int kc = 0;
+        if (item_index(0) < p.n_work) rotate_q(make_item(p, item_index(0)), 0);
+        for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
+            const Item it = make_item(p, w);
+            const int r = it.r0 + t * P + i % P;  // query row index
+            const int m = p.q_pos0 + r;           // its position
+            float m_run = -INFINITY, l_run = 0.f;
 
-        // ---- epilogue: O / l -> bf16 -> shared (TMA box layout) -> TMA store
-        mbar_wait(bar(C::kBarODone + t), 0, p.wait);
-        tc_fence_after();
-        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-        uint8_t *stile = smem + C::kQOff + t * C::kTile;
+            for (int j = 0; j < it.n_kt; ++j) {
+                mbar_wait(bar(C::kBarSFull + t), (kc + j) & 1, p.wait);
+                tc_fence_after();
+                const int kstart = 128 * (it.j_lo + j);
+                const bool full_vis = (kstart + 127 <= m) && (W == 0 || m - kstart < W);
+                const bool all_full = __all_sync(0xffffffffu, full_vis);
+                // columns [lo_c, hi_c] of this tile are visible to the row (Part 2, §10.2)
+                const int hi_c = m - kstart;
+                const int lo_c = (W > 0) ? m - W + 1 - kstart : -1000000;
+                // the whole 128-column row of S in registers
+                uint32_t v[128];
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t v[32];
-            tmem_ld32(o_addr + 32 * ch, v);
-            tmem_wait_ld();
-            uint32_t w[16];
+                for (int ch = 0; ch < 4; ++ch)
+                    tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * ch]));
+                tmem_wait_ld();
+                if (!all_full) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-                w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
-            const int bx = (32 * ch) / 64, c0 = ((32 * ch) % 64) / 8;
+                    for (int e = 0; e < 128; ++e)
+                        if (e < lo_c || e > hi_c) v[e] = __float_as_uint(-INFINITY);
+                }
+                // row max of the visible scores (8 independent chains)
+                float acc[8];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                *reinterpret_cast<uint4 *>(stile + bx * kBoxBytes + swz128(i, c0 + q4)) =
-                    make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1 + t, 128);
-        if (i == 0 && r0 + t * P < p.S_q) {
+                for (int a = 0; a < 8; ++a) acc[a] = __uint_as_float(v[a]);
 #pragma unroll
-            for (int bx = 0; bx < C::kBoxes; ++bx)
-                tma_store_3d(&tm_o, sb + C::kQOff + t * C::kTile + bx * kBoxBytes, 64 * bx, r0 + t * P, zq);
-            bulk_commit_group();
-            bulk_wait_group_read0();
+                for (int e = 8; e + 16 <= 128; e += 16)  // columns 8 .. 119
+#pragma unroll
+                    for (int a = 0; a < 8; ++a)
+                        acc[a] = fmax3(acc[a], __uint_as_float(v[e + a]), __uint_as_float(v[e + 8 + a]));
+#pragma unroll
+                for (int a = 0; a < 8; ++a) acc[a] = fmaxf(acc[a], __uint_as_float(v[120 + a]));
+                const float mx = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
+                const float m_tile = mx * p.scale_log2;
+                const float m_new = fmaxf(m_run, m_tile);
+                const bool need = (m_run != -INFINITY) && (m_new > m_run + 8.f);
+                if (__any_sync(0xffffffffu, need)) {
+                    // raise the reference max of every row of this warp and rescale O and l
+                    const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
+                    l_run *= alpha;
+                    m_run = m_new;
+#pragma unroll 1
+                    for (int ch = 0; ch < D / 16; ++ch) {
+                        uint32_t o[16];
+                        tmem_ld16(o_addr + 16 * ch, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st16(o_addr + 16 * ch, o);
+                    }
+                } else if (m_run == -INFINITY) {
+                    m_run = m_new;
+                }
+                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+
+                // p = exp2(s * log2(e)/sqrt(d) - m), row sum, P -> TMEM as bf16 over S
+                const uint64_t SC = f2_pack(p.scale_log2, p.scale_log2);
+                const uint64_t NM = f2_pack(-m_use, -m_use);
+                uint64_t lacc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        const uint64_t x = f2_pack(__uint_as_float(v[32 * q4 + 2 * e2]), __uint_as_float(v[32 * q4 + 2 * e2 + 1]));
+                        float y0, y1;
+                        f2_unpack(f2_fma(x, SC, NM), y0, y1);
+                        const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+                        lacc[e2 & 3] = f2_add(lacc[e2 & 3], f2_pack(p0, p1));
+                        pk[e2] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(s_addr + 16 * q4, pk);
+                }
+                {
+                    float a0, a1;
+                    f2_unpack(f2_add(f2_add(lacc[0], lacc[1]), f2_add(lacc[2], lacc[3])), a0, a1);
+                    l_run += a0 + a1;
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarPReady + t));
+            }
+            kc += it.n_kt;
+
+            // the next item's Q tile was loaded once this item's last QK was done:
+            // rotate it now, so its first QK overlaps this item's epilogue
+            const int w_next = item_index(k + 1);
+            if (w_next < p.n_work) rotate_q(make_item(p, w_next), k + 1);
+
+            // ---- epilogue: O / l -> bf16 -> global, one row per thread
+            mbar_wait(bar(C::kBarODone + t), k & 1, p.wait);
+            tc_fence_after();
+            const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+            const int hl = i / P;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(it.zq + hl) * p.S_q + r) * D);
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t v[32];
+                tmem_ld32(o_addr + 32 * ch, v);
+                tmem_wait_ld();
+                uint32_t w2[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w2[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+                if (r < p.S_q) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        dst[4 * ch + q4] = make_uint4(w2[4 * q4], w2[4 * q4 + 1], w2[4 * q4 + 2], w2[4 * q4 + 3]);
+                }
+            }
+            tc_fence_before();
         }
     }
 
@@ -522,7 +561,7 @@ cudaError_t launch_t(const PrefillLaunch &L, cudaStream_t stream)
     err = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
     if (err != cudaSuccess) return err;
     if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-    prefill_kernel<D><<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_o, L.p);
+    prefill_kernel<D><<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
     return cudaGetLastError();
 }
 

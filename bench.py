@@ -28,6 +28,7 @@ seed (independent problems, no collective on the data path): weak scaling.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -62,6 +63,28 @@ def decode_kv_bytes(w):
     m = w.q_pos0
     lo = max(0, m - w.window + 1) if w.window > 0 else 0
     return 2.0 * w.B * w.H_kv * (m - lo + 1) * w.d_h * 2
+
+
+def rank_workloads(rank, prefill_name=PREFILL, decode_batch=None):
+    """The step's two workloads for one rank: same shapes on every rank, seeds
+    offset by rank (independent problems, no data shared between ranks)."""
+    from transformer_attention_rope_gb300 import inputs as inp
+    wp, wd = inp.WORKLOADS[prefill_name], inp.WORKLOADS[DECODE]
+    if decode_batch:
+        wd = dataclasses.replace(wd, B=decode_batch)
+    return (dataclasses.replace(wp, seed=wp.seed + 1000 * rank),
+            dataclasses.replace(wd, seed=wd.seed + 1000 * rank))
+
+
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise maximum of a list of floats over all ranks of the default
+    process group (the slowest rank decides the job's time)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
 
 
 def load_peaks():
@@ -150,22 +173,23 @@ def bus_id_of(dev_index):
 
 
 # ---------------------------------------------------------------- CPU baseline (oracle)
-def oracle_sample_prefill(w, q, k, v, budget_rows):
-    """Oracle on batch 0, all heads, an evenly spaced subset of rows (all rows when budget_rows >= S_q)."""
+def oracle_sample_prefill(w, q, k, v, budget_rows, batches=1):
+    """Oracle on the first `batches` sequences, all heads, an evenly spaced
+    subset of rows (all rows when budget_rows >= S_q)."""
     import oracle
     step = max(1, w.S_q // budget_rows)
     rows = list(range(0, w.S_q, step))
     t0 = time.perf_counter()
-    oracle.attn(q[:1], k[:1], v[:1], window=w.window, q_pos0=w.q_pos0, rows=rows)
+    oracle.attn(q[:batches], k[:batches], v[:batches], window=w.window, q_pos0=w.q_pos0, rows=rows)
     dt = time.perf_counter() - t0
     pairs = 0
     for r in rows:
         m = w.q_pos0 + r
         lo = max(0, m - w.window + 1) if w.window > 0 else 0
         pairs += m - lo + 1
-    flops = 4.0 * w.d_h * pairs * w.H_q
-    return flops, dt, "prefill %s: batch 0 of %d, all %d heads, %d of %d rows (every %d-th)" % (
-        w.name, w.B, w.H_q, len(rows), w.S_q, step)
+    flops = 4.0 * w.d_h * pairs * w.H_q * batches
+    return flops, dt, "prefill %s: %d of %d sequences, all %d heads, %d of %d rows (every %d-th)" % (
+        w.name, batches, w.B, w.H_q, len(rows), w.S_q, step)
 
 
 def oracle_sample_decode(w, q, k, v, n_batch):
@@ -186,11 +210,9 @@ def cores_used():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(prefill_inputs, decode_inputs, rows=4096, dec_batch=32):
-    from transformer_attention_rope_gb300 import inputs as inp
-    wp, wd = inp.WORKLOADS[PREFILL], inp.WORKLOADS[DECODE]
-    fl, dtp, sp = oracle_sample_prefill(wp, *prefill_inputs, rows)
-    nb, dtd, sd = oracle_sample_decode(wd, *decode_inputs, dec_batch)
+def cpu_baseline(wp, wd, prefill_inputs, decode_inputs, rows=4096):
+    fl, dtp, sp = oracle_sample_prefill(wp, *prefill_inputs, rows, batches=wp.B)
+    nb, dtd, sd = oracle_sample_decode(wd, *decode_inputs, wd.B)
     return {"value": fl / dtp / 1e12, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
             "sample": "%s (%.1f s); %s (%.1f s)" % (sp, dtp, sd, dtd),
             "decode_value": nb / dtd / 1e9, "decode_unit": "GB/s", "seconds": dtp + dtd}
@@ -209,7 +231,7 @@ def run_reference(args):
     n_dec = 2
     dk = inp.normal_bf16((wd.B, wd.H_kv, wd.S_k, wd.d_h), wd.seed, 1)[:n_dec].contiguous()
     dv = inp.normal_bf16((wd.B, wd.H_kv, wd.S_k, wd.d_h), wd.seed, 2)[:n_dec].contiguous()
-    rows = 32
+    rows = 256
     for _ in range(args.warmup):
         oracle_sample_prefill(wp, *pin, rows)
     fl_tot = t_p = nb_tot = t_d = 0.0
@@ -240,8 +262,6 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- our arm
 def run_ours(args):
-    import dataclasses
-
     import torch
 
     import transformer_attention_rope_gb300 as apex
@@ -257,11 +277,8 @@ def run_ours(args):
         pg = dist
     apex.load_library()
 
-    wp, wd = inp.WORKLOADS[args.prefill_workload], inp.WORKLOADS[DECODE]
+    wp, wd = rank_workloads(rank, args.prefill_workload, args.decode_batch)
     do_pre, do_dec = args.part in ("all", "prefill"), args.part in ("all", "decode")
-    # every rank gets its own seeds: independent problems
-    wp = dataclasses.replace(wp, seed=wp.seed + 1000 * rank)
-    wd = dataclasses.replace(wd, seed=wd.seed + 1000 * rank)
     stream = torch.cuda.current_stream()
 
     pin = din = ()
@@ -352,14 +369,11 @@ def run_ours(args):
 
     flops = prefill_flops(wp)
     kvb = decode_kv_bytes(wd)
-    times = torch.tensor([t_pre, t_dec, t_all, te_pre, te_dec], dtype=torch.float64, device=dev)
-    if pg:
-        pg.all_reduce(times, op=pg.ReduceOp.MAX)
-    t_pre, t_dec, t_all, te_pre, te_dec = times.tolist()
+    t_pre, t_dec, t_all, te_pre, te_dec = max_over_ranks([t_pre, t_dec, t_all, te_pre, te_dec], pg, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and do_pre and do_dec:
-        cpu = cpu_baseline(pin, din)
+        cpu = cpu_baseline(wp, wd, pin, din)
 
     if rank == 0:
         peaks = load_peaks()
@@ -427,16 +441,28 @@ def run_ours(args):
 
 
 def load_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernels."""
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json),
+    only for kernels whose source is unchanged since the capture."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return {}
     try:
         with open(path) as f:
             d = json.load(f)
-        return {k: v.get("dram_bytes_per_launch") for k, v in d.items() if isinstance(v, dict)}
     except (OSError, ValueError):
         return {}
+    out = {}
+    for key, rec in d.items():
+        if not isinstance(rec, dict):
+            continue
+        try:
+            with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+                same = hashlib.sha256(f.read()).hexdigest() == rec["sha256"]
+        except (OSError, KeyError):
+            same = False
+        out[key] = rec.get("dram_bytes_per_launch") if same else None
+    return out
 
 
 def main():
@@ -449,6 +475,8 @@ def main():
     ap.add_argument("--part", choices=["all", "prefill", "decode"], default="all",
                     help="run only one of the two calls per step (profiling)")
     ap.add_argument("--prefill-workload", choices=["tiny", "gqa", "wide", "long"], default=PREFILL)
+    ap.add_argument("--decode-batch", type=int, default=None,
+                    help="decode batch size (profiling a smaller case; default: the workload's 64)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -70,14 +70,22 @@ __device__ __forceinline__ void report_status(uint32_t *status, uint32_t code)
 // at most `timeout_ns` nanoseconds.  On time-out the status word is set and
 // the caller goes on as if the wait had succeeded, so that every thread still
 // reaches every later barrier and the kernel ends (with unspecified output).
+// The global timer is read only once every 256 polls: reading it is slow, and
+// polling it on every iteration delays the wake-up after the phase completes.
 __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &wc)
 {
     if (mbar_try_wait(bar, parity)) return;
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > wc.timeout_ns) {
-            report_status(wc.status, kStatusWaitTimeout);
-            return;
+    uint64_t t0 = 0;
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return;
+        if ((n & 255u) == 0) {
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > wc.timeout_ns) {
+                report_status(wc.status, kStatusWaitTimeout);
+                return;
+            }
         }
     }
 }

@@ -40,6 +40,11 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+class _Opts(ctypes.Structure):
+    _fields_ = [("yarn_s", ctypes.c_double), ("beta_fast", ctypes.c_double), ("beta_slow", ctypes.c_double),
+                ("prefix_len", ctypes.c_int), ("keys_prerotated", ctypes.c_int)]
+
+
 def _load():
     global _lib
     with _lock:
@@ -56,6 +61,17 @@ def _load():
                 fn.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i64, f64, i32,
                                vp, i32, i32]
                 fn.restype = i32
+            for name in ("oracle_attn_ex_bf16", "oracle_attn_ex_f64"):
+                fn = getattr(lib, name)
+                fn.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i64, f64, i32,
+                               vp, i32, i32, ctypes.POINTER(_Opts)]
+                fn.restype = i32
+            lib.oracle_yarn_theta_f64.argtypes = [i32, f64, f64, f64, f64, vp]
+            lib.oracle_yarn_theta_f64.restype = i32
+            lib.oracle_yarn_scale_theta_f64.argtypes = [vp, i32, f64, f64, f64, vp]
+            lib.oracle_yarn_scale_theta_f64.restype = i32
+            lib.oracle_yarn_attn_factor.argtypes = [f64]
+            lib.oracle_yarn_attn_factor.restype = f64
             _lib = lib
     return _lib
 
@@ -93,6 +109,32 @@ def rope(x, pos, base: float = 10000.0) -> np.ndarray:
     return out.reshape(x.shape)
 
 
+def yarn_theta(d: int, base: float = 10000.0, s: float = 1.0, beta_fast: float = 32.0,
+               beta_slow: float = 1.0) -> np.ndarray:
+    """YaRN-scaled theta'_i (Part 1, §5.3-§5.4)."""
+    out = np.empty(d // 2, dtype=np.float64)
+    rc = _load().oracle_yarn_theta_f64(d, float(base), float(s), float(beta_fast), float(beta_slow), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_yarn_theta_f64: bad arguments")
+    return out
+
+
+def yarn_scale_theta(theta, s: float, beta_fast: float = 32.0, beta_slow: float = 1.0) -> np.ndarray:
+    """The YaRN rule of Part 1, §5.3-§5.4 applied to given frequencies."""
+    th = np.ascontiguousarray(np.asarray(theta, dtype=np.float64).ravel())
+    out = np.empty_like(th)
+    rc = _load().oracle_yarn_scale_theta_f64(_ptr(th), th.shape[0], float(s), float(beta_fast),
+                                             float(beta_slow), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_yarn_scale_theta_f64: bad arguments")
+    return out
+
+
+def yarn_attn_factor(s: float) -> float:
+    """Attention temperature 0.1 ln(s) + 1 (Part 1, §5.5); 1 for s <= 1."""
+    return float(_load().oracle_yarn_attn_factor(float(s)))
+
+
 def _as_bf16_bits(t) -> np.ndarray:
     """torch bf16 tensor (any device) -> contiguous uint16 numpy array of its bits."""
     import torch
@@ -102,24 +144,31 @@ def _as_bf16_bits(t) -> np.ndarray:
 
 
 def attn(q, k, v, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.0,
-         causal: bool = True, rows=None, threads: int | None = None) -> np.ndarray:
+         causal: bool = True, rows=None, threads: int | None = None, yarn_s: float = 1.0,
+         yarn_beta_fast: float = 32.0, yarn_beta_slow: float = 1.0, prefix_len: int = 0,
+         keys_prerotated: bool = False) -> np.ndarray:
     """Attention block in fp64.
 
     q [B, H_q, S_q, d]; k, v [B, H_kv, S_k, d].  bf16 torch tensors are read as
     their exact bf16 values; anything else is taken as float64.  Returns
     out [B, H_q, n_rows, d] (float64), n_rows = S_q or len(rows).
     rope_base <= 0 disables RoPE; causal=False disables the mask (both only for
-    the unmasked worked example of Part 2, §6.4).
+    the unmasked worked example of Part 2, §6.4).  yarn_s > 1 scales the RoPE
+    frequencies and the scores (Part 1, §5); prefix_len > 0 makes positions
+    [0, prefix_len) attend to each other bidirectionally (Part 2, §11.1);
+    keys_prerotated uses k as already rotated.
     """
     import torch
     bf16 = isinstance(q, torch.Tensor) and q.dtype == torch.bfloat16
     if bf16:
         qa, ka, va = _as_bf16_bits(q), _as_bf16_bits(k), _as_bf16_bits(v)
-        fn = _load().oracle_attn_bf16
+        fn = _load().oracle_attn_ex_bf16
     else:
         cv = lambda a: np.ascontiguousarray(np.asarray(a, dtype=np.float64))
         qa, ka, va = cv(q), cv(k), cv(v)
-        fn = _load().oracle_attn_f64
+        fn = _load().oracle_attn_ex_f64
+    opts = _Opts(float(yarn_s), float(yarn_beta_fast), float(yarn_beta_slow), int(prefix_len),
+                 1 if keys_prerotated else 0)
     B, H_q, S_q, d = qa.shape
     Bk, H_kv, S_k, dk = ka.shape
     if va.shape != ka.shape or Bk != B or dk != d:
@@ -132,7 +181,7 @@ def attn(q, k, v, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.
     out = np.empty((B, H_q, n_rows, d), dtype=np.float64)
     rc = fn(_ptr(qa), _ptr(ka), _ptr(va), _ptr(out), B, H_q, H_kv, S_q, S_k, d, int(window),
             int(q_pos0), float(rope_base), 1 if causal else 0, rows_ptr, n_rows,
-            int(threads or default_threads()))
+            int(threads or default_threads()), ctypes.byref(opts))
     if rc != 0:
         raise ValueError("oracle_attn failed with code %d" % rc)
     return out

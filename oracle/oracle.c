@@ -29,6 +29,18 @@
  *      M = max_j s_j ; Z = sum_j exp(s_j - M) ; o = sum_j exp(s_j - M)/Z * v_j
  *        (Part 2, §6.4 steps 3 and 4: exponentiate, normalise, weight V)
  *
+ * Options beyond the plain block (all off by default):
+ *   - YaRN frequency scaling with factor s (Part 1, §5.3-§5.4): with the
+ *     wavelength lambda_i = 2 pi / theta_i, pairs with lambda_i < beta_fast keep
+ *     theta_i, pairs with lambda_i > beta_slow * s use theta_i / s, the others
+ *     use theta_i / (t s + 1 - t) with t = (lambda_i / beta_slow - 1) / (s - 1)
+ *     clamped to [0, 1]; and the attention temperature 0.1 ln(s) + 1 multiplied
+ *     into the scores (§5.5).
+ *   - a bidirectional prefix of P positions (Part 2, §11.1): a query at m < P
+ *     sees exactly the keys j < P; queries at m >= P follow the causal/window rule.
+ *   - keys given already rotated (a KV cache holding RoPE(k, j)): the keys are
+ *     used as they are.
+ *
  * Inputs are either raw bf16 bit patterns (widened exactly to double) or
  * doubles.  A rope_base <= 0 switches RoPE off (again only for the §6.4
  * example, which has none).  The cos/sin cache of §4.7 is built here, in
@@ -40,6 +52,9 @@
  * thread count.
  */
 #include <math.h>
+#ifndef M_PI
+#define M_PI 3.14159265358979323846
+#endif
 #include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -70,6 +85,44 @@ static double rope_theta(int i, int d, double base)
     return pow(base, -2.0 * (double)i / (double)d);
 }
 
+typedef struct {
+    double yarn_s;      /* YaRN scale factor s; <= 1: no scaling */
+    double beta_fast;   /* wavelength below which a pair is not scaled (32)  */
+    double beta_slow;   /* beta_slow * s: wavelength above which it is fully scaled (1) */
+    int prefix_len;     /* P: bidirectional prefix [0, P); 0: none */
+    int keys_prerotated;/* keys already carry their rotation */
+} oracle_opts;
+
+/* Part 1, §5.3-§5.4: the YaRN-scaled value of one frequency theta. */
+static double yarn_scale(double th, const oracle_opts *o)
+{
+    if (!o || o->yarn_s <= 1.0)
+        return th;
+    const double s = o->yarn_s;
+    const double lambda = 2.0 * M_PI / th;           /* wavelength */
+    if (lambda < o->beta_fast)                       /* high frequency: unchanged */
+        return th;
+    if (lambda > o->beta_slow * s)                   /* low frequency: full scaling */
+        return th / s;
+    double t = (lambda / o->beta_slow - 1.0) / (s - 1.0);  /* mid: interpolate */
+    if (t < 0.0) t = 0.0;
+    if (t > 1.0) t = 1.0;
+    return th / (t * s + (1.0 - t));
+}
+
+static double yarn_theta(int i, int d, double base, const oracle_opts *o)
+{
+    return yarn_scale(rope_theta(i, d, base), o);
+}
+
+/* Part 1, §5.5: attention temperature, multiplied into the scores. */
+static double yarn_attn_factor(const oracle_opts *o)
+{
+    if (!o || o->yarn_s <= 1.0)
+        return 1.0;
+    return 0.1 * log(o->yarn_s) + 1.0;
+}
+
 /* Part 1, §4.7: cos/sin cache, one (cos, sin) pair per (position, pair i). */
 typedef struct {
     long n_pos;
@@ -77,7 +130,7 @@ typedef struct {
     double *cs; /* [n_pos][half][2] */
 } rope_cache;
 
-static int rope_cache_build(rope_cache *c, long n_pos, int d, double base)
+static int rope_cache_build(rope_cache *c, long n_pos, int d, double base, const oracle_opts *o)
 {
     c->n_pos = n_pos;
     c->half = d / 2;
@@ -88,7 +141,7 @@ static int rope_cache_build(rope_cache *c, long n_pos, int d, double base)
     if (!c->cs)
         return ORACLE_ERR_NOMEM;
     for (int i = 0; i < c->half; ++i) {
-        double th = rope_theta(i, d, base);
+        double th = yarn_theta(i, d, base, o);
         for (long m = 0; m < n_pos; ++m) {
             double ang = (double)m * th;
             c->cs[((size_t)m * c->half + i) * 2 + 0] = cos(ang);
@@ -119,11 +172,14 @@ static void rope_apply(const rope_cache *c, long m, const double *x, double *out
     }
 }
 
-/* Part 2, §10.2 (with the causal part of the same formula). */
-static int key_visible(long m, long j, int window, int causal)
+/* Part 2, §10.2 (with the causal part of the same formula), and the
+ * bidirectional prefix of Part 2, §11.1. */
+static int key_visible(long m, long j, int window, int causal, int prefix_len)
 {
     if (!causal)
         return 1;
+    if (m < prefix_len)
+        return j < prefix_len;
     if (j > m)
         return 0;
     if (window > 0 && m - j >= (long)window)
@@ -136,7 +192,8 @@ typedef struct {
     const void *q, *k, *v;
     int kind;
     double *out;
-    int B, H_q, H_kv, S_q, S_k, d, window, causal;
+    int B, H_q, H_kv, S_q, S_k, d, window, causal, prefix_len, keys_prerotated;
+    double score_factor; /* 1 / sqrt(d_h), times the YaRN temperature */
     long q_pos0;
     const int *rows;
     int n_rows;
@@ -174,22 +231,27 @@ static void run_task(attn_job *job, long task, double *kbuf, double *qraw, doubl
     const int b = (int)(task / ((long)job->n_chunks * job->H_kv));
     const int i0 = chunk_id * job->chunk;
     const int i1 = (i0 + job->chunk < job->n_rows) ? i0 + job->chunk : job->n_rows;
-    const double inv_sqrt_d = 1.0 / sqrt((double)d);
+    const double score_factor = job->score_factor;
 
-    /* keys this chunk can see: every key, narrowed by the causal/window bound */
+    /* keys this chunk can see: the union of its rows' visible ranges */
     long j_lo = 0, j_hi = job->S_k - 1;
     if (job->causal) {
-        long m_lo = -1, m_hi = -1;
+        long lo_all = job->S_k, hi_all = -1;
         for (int i = i0; i < i1; ++i) {
             long m = job->q_pos0 + row_index(job, i);
-            if (m_lo < 0 || m < m_lo) m_lo = m;
-            if (m > m_hi) m_hi = m;
+            long lo, hi;
+            if (m < job->prefix_len) {
+                lo = 0;
+                hi = job->prefix_len - 1;
+            } else {
+                hi = m;
+                lo = (job->window > 0 && m - job->window + 1 > 0) ? m - job->window + 1 : 0;
+            }
+            if (lo < lo_all) lo_all = lo;
+            if (hi > hi_all) hi_all = hi;
         }
-        j_hi = m_hi < j_hi ? m_hi : j_hi;
-        if (job->window > 0) {
-            long lo = m_lo - job->window + 1;
-            j_lo = lo > 0 ? lo : 0;
-        }
+        j_lo = lo_all;
+        if (hi_all < j_hi) j_hi = hi_all;
     }
 
     /* step 3 for the keys: k'_j = RoPE(k_j, j) */
@@ -198,7 +260,10 @@ static void run_task(attn_job *job, long task, double *kbuf, double *qraw, doubl
         size_t base = (kv_head * job->S_k + (size_t)j) * d;
         for (int e = 0; e < d; ++e)
             kraw[e] = load_elem(job->k, base + e, job->kind);
-        rope_apply(job->cache, j, kraw, kbuf + (size_t)(j - j_lo) * d, d);
+        if (job->keys_prerotated)
+            memcpy(kbuf + (size_t)(j - j_lo) * d, kraw, sizeof(double) * (size_t)d);
+        else
+            rope_apply(job->cache, j, kraw, kbuf + (size_t)(j - j_lo) * d, d);
     }
 
     for (int hh = 0; hh < G; ++hh) {
@@ -211,17 +276,17 @@ static void run_task(attn_job *job, long task, double *kbuf, double *qraw, doubl
                 qraw[e] = load_elem(job->q, qbase + e, job->kind);
             rope_apply(job->cache, m, qraw, qrot, d);
 
-            /* step 4: scaled scores of the visible keys */
+            /* step 4: scaled scores of the visible keys (times the YaRN temperature) */
             double M = -INFINITY;
             int any = 0;
             for (long j = j_lo; j <= j_hi; ++j) {
-                if (!key_visible(m, j, job->window, job->causal))
+                if (!key_visible(m, j, job->window, job->causal, job->prefix_len))
                     continue;
                 const double *kr = kbuf + (size_t)(j - j_lo) * d;
                 double dot = 0.0;
                 for (int e = 0; e < d; ++e)
                     dot += qrot[e] * kr[e];
-                double s = dot * inv_sqrt_d;
+                double s = dot * score_factor;
                 scores[j - j_lo] = s;
                 if (!any || s > M) M = s;
                 any = 1;
@@ -234,11 +299,11 @@ static void run_task(attn_job *job, long task, double *kbuf, double *qraw, doubl
             /* step 5: Z = sum exp(s - M), then o = sum exp(s - M)/Z * v */
             double Z = 0.0;
             for (long j = j_lo; j <= j_hi; ++j)
-                if (key_visible(m, j, job->window, job->causal))
+                if (key_visible(m, j, job->window, job->causal, job->prefix_len))
                     Z += exp(scores[j - j_lo] - M);
             for (int e = 0; e < d; ++e) acc[e] = 0.0;
             for (long j = j_lo; j <= j_hi; ++j) {
-                if (!key_visible(m, j, job->window, job->causal))
+                if (!key_visible(m, j, job->window, job->causal, job->prefix_len))
                     continue;
                 double p = exp(scores[j - j_lo] - M) / Z;
                 size_t vbase = (kv_head * job->S_k + (size_t)j) * d;
@@ -280,8 +345,11 @@ static void *worker(void *arg)
 static int attn_common(const void *q, const void *k, const void *v, int kind, double *out,
                        int B, int H_q, int H_kv, int S_q, int S_k, int d, int window,
                        long q_pos0, double rope_base, int causal, const int *rows, int n_rows,
-                       int n_threads)
+                       int n_threads, const oracle_opts *opts)
 {
+    if (opts && (opts->prefix_len < 0 || opts->prefix_len > S_k ||
+                 (opts->yarn_s > 1.0 && (opts->beta_fast <= 0.0 || opts->beta_slow <= 0.0))))
+        return ORACLE_ERR_ARG;
     if (!q || !k || !v || !out || B <= 0 || H_q <= 0 || H_kv <= 0 || S_q <= 0 || S_k <= 0 ||
         d <= 0 || (d & 1) || H_q % H_kv != 0 || q_pos0 < 0)
         return ORACLE_ERR_ARG;
@@ -299,7 +367,7 @@ static int attn_common(const void *q, const void *k, const void *v, int kind, do
     }
 
     rope_cache cache;
-    if (rope_cache_build(&cache, max_pos, d, rope_base) != ORACLE_OK)
+    if (rope_cache_build(&cache, max_pos, d, rope_base, opts) != ORACLE_OK)
         return ORACLE_ERR_NOMEM;
 
     attn_job job;
@@ -307,6 +375,9 @@ static int attn_common(const void *q, const void *k, const void *v, int kind, do
     job.q = q; job.k = k; job.v = v; job.kind = kind; job.out = out;
     job.B = B; job.H_q = H_q; job.H_kv = H_kv; job.S_q = S_q; job.S_k = S_k; job.d = d;
     job.window = window; job.causal = causal; job.q_pos0 = q_pos0;
+    job.prefix_len = opts ? opts->prefix_len : 0;
+    job.keys_prerotated = opts ? opts->keys_prerotated : 0;
+    job.score_factor = yarn_attn_factor(opts) / sqrt((double)d);
     job.rows = rows; job.n_rows = n_rows; job.cache = &cache;
     if (n_threads <= 0)
         n_threads = 1;
@@ -380,14 +451,33 @@ int oracle_rope_theta_f64(int d, double base, double *theta)
  *   q   [B, H_q,  S_q, d]      k, v [B, H_kv, S_k, d]     (row-major)
  *   out [B, H_q,  n_rows, d]   doubles; n_rows = S_q when rows == NULL,
  *                              otherwise row i of out is query row rows[i].
+ * The _ex forms take the options above (NULL: none).
  */
+int oracle_attn_ex_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *out,
+                        int B, int H_q, int H_kv, int S_q, int S_k, int d, int window,
+                        long q_pos0, double rope_base, int causal, const int *rows, int n_rows,
+                        int n_threads, const oracle_opts *opts)
+{
+    return attn_common(q, k, v, ELEM_BF16, out, B, H_q, H_kv, S_q, S_k, d, window, q_pos0,
+                       rope_base, causal, rows, n_rows, n_threads, opts);
+}
+
+int oracle_attn_ex_f64(const double *q, const double *k, const double *v, double *out, int B,
+                       int H_q, int H_kv, int S_q, int S_k, int d, int window, long q_pos0,
+                       double rope_base, int causal, const int *rows, int n_rows, int n_threads,
+                       const oracle_opts *opts)
+{
+    return attn_common(q, k, v, ELEM_F64, out, B, H_q, H_kv, S_q, S_k, d, window, q_pos0,
+                       rope_base, causal, rows, n_rows, n_threads, opts);
+}
+
 int oracle_attn_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *out,
                      int B, int H_q, int H_kv, int S_q, int S_k, int d, int window,
                      long q_pos0, double rope_base, int causal, const int *rows, int n_rows,
                      int n_threads)
 {
     return attn_common(q, k, v, ELEM_BF16, out, B, H_q, H_kv, S_q, S_k, d, window, q_pos0,
-                       rope_base, causal, rows, n_rows, n_threads);
+                       rope_base, causal, rows, n_rows, n_threads, NULL);
 }
 
 /* The same on double inputs (worked examples and brute-force checks). */
@@ -396,5 +486,47 @@ int oracle_attn_f64(const double *q, const double *k, const double *v, double *o
                     double rope_base, int causal, const int *rows, int n_rows, int n_threads)
 {
     return attn_common(q, k, v, ELEM_F64, out, B, H_q, H_kv, S_q, S_k, d, window, q_pos0,
-                       rope_base, causal, rows, n_rows, n_threads);
+                       rope_base, causal, rows, n_rows, n_threads, NULL);
+}
+
+/* YaRN-scaled frequencies theta'_i, i < d/2 (Part 1, §5.3-§5.4), and the
+ * attention temperature (§5.5). */
+int oracle_yarn_theta_f64(int d, double base, double s, double beta_fast, double beta_slow,
+                          double *theta)
+{
+    if (d <= 0 || (d & 1) || base <= 0.0 || !theta || beta_fast <= 0.0 || beta_slow <= 0.0)
+        return ORACLE_ERR_ARG;
+    oracle_opts o;
+    memset(&o, 0, sizeof o);
+    o.yarn_s = s;
+    o.beta_fast = beta_fast;
+    o.beta_slow = beta_slow;
+    for (int i = 0; i < d / 2; ++i)
+        theta[i] = yarn_theta(i, d, base, &o);
+    return ORACLE_OK;
+}
+
+/* The YaRN rule applied to arbitrary frequencies (the worked example of
+ * Part 1, §5.6 quotes rounded theta values). */
+int oracle_yarn_scale_theta_f64(const double *theta, int n, double s, double beta_fast,
+                                double beta_slow, double *out)
+{
+    if (!theta || !out || n < 0 || beta_fast <= 0.0 || beta_slow <= 0.0)
+        return ORACLE_ERR_ARG;
+    oracle_opts o;
+    memset(&o, 0, sizeof o);
+    o.yarn_s = s;
+    o.beta_fast = beta_fast;
+    o.beta_slow = beta_slow;
+    for (int i = 0; i < n; ++i)
+        out[i] = yarn_scale(theta[i], &o);
+    return ORACLE_OK;
+}
+
+double oracle_yarn_attn_factor(double s)
+{
+    oracle_opts o;
+    memset(&o, 0, sizeof o);
+    o.yarn_s = s;
+    return yarn_attn_factor(&o);
 }

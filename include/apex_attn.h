@@ -84,6 +84,65 @@ apex_status apex_attn_fwd(const void *q, const void *k, const void *v, void *out
                           int window, int q_pos0, float rope_base, apex_stream_t stream);
 
 /*
+ * Options of the _ex entry points.  Zero-initialise the struct and set what is
+ * needed: all zeros is the plain block with rope_base 10000.
+ */
+typedef struct apex_attn_options {
+    int window;           /* <= 0: causal only; > 0: sliding window W            */
+    int q_pos;            /* fwd: position of query row 0; decode: the query's   */
+    float rope_base;      /* RoPE base b of theta_i = b^(-2i/d_h); 0 means 10000 */
+    float yarn_scale;     /* YaRN factor s (Part 1 §5); <= 1: no YaRN            */
+    float yarn_beta_fast; /* wavelength below which a pair is unscaled; 0: 32    */
+    float yarn_beta_slow; /* beta_slow * s: wavelength above which theta/s; 0: 1 */
+    int prefix_len;       /* P > 0: positions [0, P) attend to each other
+                             bidirectionally (Part 2 §11.1); 0 <= P <= S_k       */
+    int keys_prerotated;  /* non-zero: k / k_cache already hold RoPE(k_j, j)     */
+} apex_attn_options;
+
+/*
+ * YaRN (Part 1 §5.3-§5.5), when yarn_scale > 1: with the wavelength
+ * lambda_i = 2 pi / theta_i, pairs with lambda_i < beta_fast keep theta_i,
+ * pairs with lambda_i > beta_slow * s use theta_i / s, the others use
+ * theta_i / (t s + 1 - t), t = clamp((lambda_i / beta_slow - 1) / (s - 1), 0, 1);
+ * the scores are multiplied by 0.1 ln(s) + 1.
+ * Prefix (Part 2 §11.1), when prefix_len = P > 0: a query at m < P sees the keys
+ * j < P and nothing else; queries at m >= P follow the causal/window rule.
+ */
+
+/*
+ * Prefill with options: as apex_attn_fwd, with window, q_pos0 (= opt->q_pos)
+ * and rope_base taken from *opt.  opt may not be NULL.
+ */
+apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *out,
+                             int B, int H_q, int H_kv, int S_q, int S_k, int d_h,
+                             const apex_attn_options *opt, apex_stream_t stream);
+
+/*
+ * Decode with options: as apex_attn_decode, with window, q_pos and rope_base
+ * taken from *opt.  With a prefix and q_pos < P the query sees keys [0, P).
+ * The workspace size is apex_attn_decode_workspace_bytes(...) as for
+ * apex_attn_decode.
+ */
+apex_status apex_attn_decode_ex(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                int B, int H_q, int H_kv, int S_k, int d_h,
+                                const apex_attn_options *opt, void *workspace,
+                                size_t workspace_bytes, apex_stream_t stream);
+
+/*
+ * Rotate keys for a pre-rotated KV cache (Part 1 §4.2-§4.4, with the options'
+ * rope_base / YaRN): for each of n_heads heads h and each s < n_pos,
+ *   k_out[h * out_head_stride + s * d_h + :] = RoPE(k_in[h * in_head_stride + s * d_h + :], pos0 + s)
+ * in bf16 (fp32 arithmetic).  Strides are in elements; with
+ * out_head_stride = S_cache * d_h and k_out pointing at row pos0 of a cache,
+ * this appends freshly projected keys to that cache.  k_out may equal k_in
+ * (same strides) for an in-place rotation; otherwise the ranges must not
+ * overlap.  Only window/prefix-independent fields of *opt are used.
+ */
+apex_status apex_attn_rope_keys(const void *k_in, void *k_out, int n_heads, int n_pos, int d_h, int pos0,
+                                long long in_head_stride, long long out_head_stride,
+                                const apex_attn_options *opt, apex_stream_t stream);
+
+/*
  * Bytes of caller-provided device workspace apex_attn_decode needs for these
  * sizes (the split-KV partial results).  Returns 0 when the sizes are invalid.
  * The same sizes with any window / q_pos never need more.

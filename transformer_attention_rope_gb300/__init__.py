@@ -7,9 +7,10 @@ There is no CPU fallback -- if the library is missing, every call raises.
 
 Raw C-ABI names (pointers and sizes):
     apex_attn_fwd, apex_attn_decode, apex_attn_decode_noalloc, apex_attn_decode_workspace_bytes,
-    apex_attn_rope_reserve, apex_attn_device_status, apex_attn_status_string
+    apex_attn_rope_reserve, apex_attn_device_status, apex_attn_status_string,
+    apex_attn_fwd_ex, apex_attn_decode_ex, apex_attn_rope_keys (with an Options struct)
 Tensor conveniences (torch, bf16, contiguous, on the current CUDA device):
-    fwd(q, k, v, ...), decode(q, k_cache, v_cache, q_pos, ...)
+    fwd(q, k, v, ...), decode(q, k_cache, v_cache, q_pos, ...), rope_keys(k, ...)
 """
 from __future__ import annotations
 
@@ -20,7 +21,8 @@ import threading
 __all__ = [
     "ApexError", "library_path", "load_library", "apex_attn_fwd", "apex_attn_decode", "apex_attn_decode_noalloc",
     "apex_attn_decode_workspace_bytes", "apex_attn_rope_reserve", "apex_attn_device_status",
-    "apex_attn_status_string", "fwd", "decode", "decode_workspace_bytes",
+    "apex_attn_status_string", "apex_attn_fwd_ex", "apex_attn_decode_ex", "apex_attn_rope_keys", "Options",
+    "fwd", "decode", "decode_workspace_bytes", "rope_keys",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -31,6 +33,13 @@ _lib = None
 APEX_OK = 0
 _STATUS_NAMES = {0: "APEX_OK", 1: "APEX_ERR_INVALID_ARG", 2: "APEX_ERR_UNSUPPORTED", 3: "APEX_ERR_CUDA",
                  4: "APEX_ERR_NO_MEMORY", 5: "APEX_ERR_DEVICE_TIMEOUT"}
+
+
+class Options(ctypes.Structure):
+    """apex_attn_options of include/apex_attn.h (all zeros: the plain block)."""
+    _fields_ = [("window", ctypes.c_int), ("q_pos", ctypes.c_int), ("rope_base", ctypes.c_float),
+                ("yarn_scale", ctypes.c_float), ("yarn_beta_fast", ctypes.c_float),
+                ("yarn_beta_slow", ctypes.c_float), ("prefix_len", ctypes.c_int), ("keys_prerotated", ctypes.c_int)]
 
 
 class ApexError(RuntimeError):
@@ -60,6 +69,13 @@ def load_library():
             lib.apex_attn_decode.restype = i32
             lib.apex_attn_decode_noalloc.argtypes = [vp, vp, vp, vp] + [i32] * 7 + [f32, vp]
             lib.apex_attn_decode_noalloc.restype = i32
+            op = ctypes.POINTER(Options)
+            lib.apex_attn_fwd_ex.argtypes = [vp, vp, vp, vp] + [i32] * 6 + [op, vp]
+            lib.apex_attn_fwd_ex.restype = i32
+            lib.apex_attn_decode_ex.argtypes = [vp, vp, vp, vp] + [i32] * 5 + [op, vp, sz, vp]
+            lib.apex_attn_decode_ex.restype = i32
+            lib.apex_attn_rope_keys.argtypes = [vp, vp] + [i32] * 4 + [ctypes.c_longlong] * 2 + [op, vp]
+            lib.apex_attn_rope_keys.restype = i32
             lib.apex_attn_decode_workspace_bytes.argtypes = [i32] * 5
             lib.apex_attn_decode_workspace_bytes.restype = sz
             lib.apex_attn_rope_reserve.argtypes = [i32, i32, f32]
@@ -88,6 +104,25 @@ def apex_attn_decode_noalloc(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, w
                              stream) -> int:
     return load_library().apex_attn_decode_noalloc(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, window,
                                                    q_pos, rope_base, stream)
+
+
+def apex_attn_fwd_ex(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, opt, stream) -> int:
+    return load_library().apex_attn_fwd_ex(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h,
+                                           ctypes.byref(opt) if opt is not None else None, stream)
+
+
+def apex_attn_decode_ex(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, opt, workspace, workspace_bytes,
+                        stream) -> int:
+    return load_library().apex_attn_decode_ex(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h,
+                                              ctypes.byref(opt) if opt is not None else None, workspace,
+                                              workspace_bytes, stream)
+
+
+def apex_attn_rope_keys(k_in, k_out, n_heads, n_pos, d_h, pos0, in_head_stride, out_head_stride, opt,
+                        stream) -> int:
+    return load_library().apex_attn_rope_keys(k_in, k_out, n_heads, n_pos, d_h, pos0, in_head_stride,
+                                              out_head_stride, ctypes.byref(opt) if opt is not None else None,
+                                              stream)
 
 
 def apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_h) -> int:
@@ -121,7 +156,15 @@ def _stream_handle(stream):
     return s.cuda_stream
 
 
-def fwd(q, k, v, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.0, out=None, stream=None):
+def _options(window=0, q_pos=0, rope_base=10000.0, yarn_scale=1.0, yarn_beta_fast=32.0, yarn_beta_slow=1.0,
+             prefix_len=0, keys_prerotated=False) -> Options:
+    return Options(int(window), int(q_pos), float(rope_base), float(yarn_scale), float(yarn_beta_fast),
+                   float(yarn_beta_slow), int(prefix_len), 1 if keys_prerotated else 0)
+
+
+def fwd(q, k, v, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.0, out=None, stream=None,
+        yarn_scale: float = 1.0, yarn_beta_fast: float = 32.0, yarn_beta_slow: float = 1.0, prefix_len: int = 0,
+        keys_prerotated: bool = False):
     """Prefill. q [B,H_q,S_q,d], k/v [B,H_kv,S_k,d] (bf16, CUDA) -> out [B,H_q,S_q,d]."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -131,8 +174,15 @@ def fwd(q, k, v, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.0
     if out is None:
         out = torch.empty_like(q)
     _check(out, "out", 4)
-    st = apex_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H_q, H_kv, S_q, S_k, d,
-                       int(window), int(q_pos0), float(rope_base), _stream_handle(stream))
+    plain = yarn_scale <= 1.0 and prefix_len == 0 and not keys_prerotated
+    if plain:
+        st = apex_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H_q, H_kv, S_q, S_k, d,
+                           int(window), int(q_pos0), float(rope_base), _stream_handle(stream))
+    else:
+        opt = _options(window, q_pos0, rope_base, yarn_scale, yarn_beta_fast, yarn_beta_slow, prefix_len,
+                       keys_prerotated)
+        st = apex_attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H_q, H_kv, S_q, S_k,
+                              d, opt, _stream_handle(stream))
     if st != APEX_OK:
         raise ApexError(st, "apex_attn_fwd")
     return out
@@ -143,7 +193,8 @@ def decode_workspace_bytes(B, H_q, H_kv, S_k, d_h) -> int:
 
 
 def decode(q, k_cache, v_cache, q_pos: int, *, window: int = 0, rope_base: float = 10000.0, out=None,
-           workspace=None, stream=None):
+           workspace=None, stream=None, yarn_scale: float = 1.0, yarn_beta_fast: float = 32.0,
+           yarn_beta_slow: float = 1.0, prefix_len: int = 0, keys_prerotated: bool = False):
     """Decode. q [B,H_q,1,d], caches [B,H_kv,S_k,d] (bf16, CUDA) -> out [B,H_q,1,d]."""
     import torch
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
@@ -158,9 +209,36 @@ def decode(q, k_cache, v_cache, q_pos: int, *, window: int = 0, rope_base: float
     need = decode_workspace_bytes(B, H_q, H_kv, S_k, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    st = apex_attn_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), B, H_q, H_kv,
-                          S_k, d, int(window), int(q_pos), float(rope_base), workspace.data_ptr(),
-                          workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    ws_bytes = workspace.numel() * workspace.element_size()
+    plain = yarn_scale <= 1.0 and prefix_len == 0 and not keys_prerotated
+    if plain:
+        st = apex_attn_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), B, H_q, H_kv,
+                              S_k, d, int(window), int(q_pos), float(rope_base), workspace.data_ptr(), ws_bytes,
+                              _stream_handle(stream))
+    else:
+        opt = _options(window, q_pos, rope_base, yarn_scale, yarn_beta_fast, yarn_beta_slow, prefix_len,
+                       keys_prerotated)
+        st = apex_attn_decode_ex(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), B, H_q,
+                                 H_kv, S_k, d, opt, workspace.data_ptr(), ws_bytes, _stream_handle(stream))
     if st != APEX_OK:
         raise ApexError(st, "apex_attn_decode")
+    return out
+
+
+def rope_keys(k, *, pos0: int = 0, out=None, rope_base: float = 10000.0, yarn_scale: float = 1.0,
+              yarn_beta_fast: float = 32.0, yarn_beta_slow: float = 1.0, stream=None):
+    """Rotate keys k [B,H,S,d] (bf16, CUDA) to positions pos0 + s: out = RoPE(k) (pre-rotated cache)."""
+    import torch
+    _check(k, "k", 4)
+    B, H, S, d = k.shape
+    if out is None:
+        out = torch.empty_like(k)
+    _check(out, "out", 4)
+    if out.shape != k.shape:
+        raise ValueError("out must have the shape of k")
+    opt = _options(0, 0, rope_base, yarn_scale, yarn_beta_fast, yarn_beta_slow)
+    st = apex_attn_rope_keys(k.data_ptr(), out.data_ptr(), B * H, S, d, int(pos0), S * d, S * d, opt,
+                             _stream_handle(stream))
+    if st != APEX_OK:
+        raise ApexError(st, "apex_attn_rope_keys")
     return out

@@ -20,9 +20,18 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSeq = 1 << 24;
 
+// RoPE frequency parameters: base and the YaRN scaling (s <= 1: none).
+struct RopeFreq {
+    float base, yarn_s, beta_fast, beta_slow;
+    bool operator==(const RopeFreq &o) const
+    {
+        return base == o.base && yarn_s == o.yarn_s && beta_fast == o.beta_fast && beta_slow == o.beta_slow;
+    }
+};
+
 struct RopeTable {
     int d_h;
-    float base;
+    RopeFreq f;
     float2 *dev;
     int cap;  // positions held
 };
@@ -60,14 +69,32 @@ apex_status init_device(DeviceState &st, int dev)
     return APEX_OK;
 }
 
-// Part 1, §4.3 and §4.7: theta_i = base^(-2i/d_h) and the (cos, sin) cache of
-// m * theta_i for every position m, computed in double precision and stored as
-// fp32 pairs [cap][d_h/2].
-apex_status get_table(DeviceState &st, int d_h, float base, int need, RopeTableView *out)
+// Part 1, §4.3: theta_i = base^(-2i/d_h); with YaRN (Part 1, §5.3-§5.4) the
+// pair's wavelength 2 pi / theta_i decides: below beta_fast it is kept, above
+// beta_slow * s it is divided by s, in between divided by t s + 1 - t with
+// t = (wavelength / beta_slow - 1) / (s - 1) clamped to [0, 1].
+double rope_frequency(int i, int d_h, const RopeFreq &f)
+{
+    const double theta = pow((double)f.base, -2.0 * (double)i / (double)d_h);
+    if (!(f.yarn_s > 1.f)) return theta;
+    const double s = f.yarn_s, lambda = 2.0 * 3.14159265358979323846 / theta;
+    if (lambda < f.beta_fast) return theta;
+    if (lambda > (double)f.beta_slow * s) return theta / s;
+    double t = (lambda / f.beta_slow - 1.0) / (s - 1.0);
+    t = t < 0.0 ? 0.0 : (t > 1.0 ? 1.0 : t);
+    return theta / (t * s + (1.0 - t));
+}
+
+// Part 1, §5.5: the YaRN attention temperature multiplied into the scores.
+double score_temperature(const RopeFreq &f) { return f.yarn_s > 1.f ? 0.1 * log((double)f.yarn_s) + 1.0 : 1.0; }
+
+// Part 1, §4.7: the (cos, sin) cache of m * theta_i for every position m,
+// computed in double precision and stored as fp32 pairs [cap][d_h/2].
+apex_status get_table(DeviceState &st, int d_h, const RopeFreq &f, int need, RopeTableView *out)
 {
     need = std::max(need, 128);
     for (auto &t : st.tables) {
-        if (t.d_h == d_h && t.base == base && t.cap >= need) {
+        if (t.d_h == d_h && t.f == f && t.cap >= need) {
             *out = RopeTableView{t.dev, t.cap};
             return APEX_OK;
         }
@@ -77,7 +104,7 @@ apex_status get_table(DeviceState &st, int d_h, float base, int need, RopeTableV
     const int half = d_h / 2;
     std::vector<float2> host((size_t)cap * half);
     for (int i = 0; i < half; ++i) {
-        const double theta = pow((double)base, -2.0 * (double)i / (double)d_h);
+        const double theta = rope_frequency(i, d_h, f);
         for (int m = 0; m < cap; ++m) {
             const double a = (double)m * theta;
             host[(size_t)m * half + i] = make_float2((float)cos(a), (float)sin(a));
@@ -92,18 +119,33 @@ apex_status get_table(DeviceState &st, int d_h, float base, int need, RopeTableV
         cudaFree(dev);
         return APEX_ERR_CUDA;
     }
-    // replace a smaller table of the same (d_h, base); cudaFree waits for the
+    // replace a smaller table of the same parameters; cudaFree waits for the
     // device, so no kernel still reads the old one
     for (auto it = st.tables.begin(); it != st.tables.end(); ++it) {
-        if (it->d_h == d_h && it->base == base) {
+        if (it->d_h == d_h && it->f == f) {
             cudaFree(it->dev);
             st.tables.erase(it);
             break;
         }
     }
-    st.tables.push_back(RopeTable{d_h, base, dev, cap});
+    st.tables.push_back(RopeTable{d_h, f, dev, cap});
     *out = RopeTableView{dev, cap};
     return APEX_OK;
+}
+
+// Options -> frequency parameters, with the documented defaults; false when invalid.
+bool freq_of(const apex_attn_options &o, RopeFreq *f)
+{
+    f->base = o.rope_base == 0.f ? 10000.f : o.rope_base;
+    f->yarn_s = o.yarn_scale > 1.f ? o.yarn_scale : 1.f;
+    f->beta_fast = o.yarn_beta_fast == 0.f ? 32.f : o.yarn_beta_fast;
+    f->beta_slow = o.yarn_beta_slow == 0.f ? 1.f : o.yarn_beta_slow;
+    if (!(f->base > 0.f) || !isfinite(f->base)) return false;
+    if (!isfinite(o.yarn_scale) || !isfinite(f->yarn_s)) return false;
+    if (f->yarn_s > 1.f && (!(f->beta_fast > 0.f) || !(f->beta_slow > 0.f) || !isfinite(f->beta_fast) ||
+                            !isfinite(f->beta_slow)))
+        return false;
+    return true;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -231,7 +273,7 @@ apex_status apex_attn_rope_reserve(int max_pos, int d_h, float rope_base)
     apex_status s = init_device(*st, dev);
     if (s != APEX_OK) return s;
     RopeTableView tv;
-    return get_table(*st, d_h, rope_base, max_pos, &tv);
+    return get_table(*st, d_h, RopeFreq{rope_base, 1.f, 32.f, 1.f}, max_pos, &tv);
 }
 
 apex_status apex_attn_device_status(void)
@@ -260,16 +302,20 @@ size_t apex_attn_decode_workspace_bytes(int B, int H_q, int H_kv, int S_k, int d
     return bytes + rows * sizeof(float2);
 }
 
-apex_status apex_attn_decode(const void *q, const void *k_cache, const void *v_cache, void *out, int B, int H_q,
-                             int H_kv, int S_k, int d_h, int window, int q_pos, float rope_base, void *workspace,
-                             size_t workspace_bytes, apex_stream_t stream)
+apex_status apex_attn_decode_ex(const void *q, const void *k_cache, const void *v_cache, void *out, int B, int H_q,
+                                int H_kv, int S_k, int d_h, const apex_attn_options *opt, void *workspace,
+                                size_t workspace_bytes, apex_stream_t stream)
 {
-    if (!q || !k_cache || !v_cache || !out || !workspace) return APEX_ERR_INVALID_ARG;
+    if (!q || !k_cache || !v_cache || !out || !workspace || !opt) return APEX_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
         return APEX_ERR_INVALID_ARG;
-    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, rope_base);
+    RopeFreq f;
+    if (!freq_of(*opt, &f)) return APEX_ERR_INVALID_ARG;
+    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, f.base);
     if (s != APEX_OK) return s;
+    const int q_pos = opt->q_pos, window = opt->window, P = opt->prefix_len;
     if (q_pos < 0 || q_pos >= S_k) return APEX_ERR_INVALID_ARG;
+    if (P < 0 || P > S_k) return APEX_ERR_INVALID_ARG;
     const size_t need = apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_h);
     if (workspace_bytes < need) return APEX_ERR_INVALID_ARG;
 
@@ -280,7 +326,7 @@ apex_status apex_attn_decode(const void *q, const void *k_cache, const void *v_c
     s = init_device(*st, dev);
     if (s != APEX_OK) return s;
     RopeTableView tv;
-    s = get_table(*st, d_h, rope_base, S_k, &tv);
+    s = get_table(*st, d_h, f, S_k, &tv);
     if (s != APEX_OK) return s;
 
     DecodeLaunch L;
@@ -306,28 +352,54 @@ apex_status apex_attn_decode(const void *q, const void *k_cache, const void *v_c
     p.S_k = S_k;
     p.d_h = d_h;
     p.q_pos = q_pos;
-    p.k_lo = (window > 0) ? std::max(0, q_pos - window + 1) : 0;
+    // visible keys (Part 2, §10.2; a query inside the prefix sees the whole prefix, §11.1)
+    if (q_pos < P) {
+        p.k_lo = 0;
+        p.k_hi = P - 1;
+    } else {
+        p.k_lo = (window > 0) ? std::max(0, q_pos - window + 1) : 0;
+        p.k_hi = q_pos;
+    }
     p.stage0 = p.k_lo / kDecodeKeysPerStage;
-    p.n_stages = q_pos / kDecodeKeysPerStage - p.stage0 + 1;
+    p.n_stages = p.k_hi / kDecodeKeysPerStage - p.stage0 + 1;
     const int capacity = decode_ctas_per_sm(d_h, p.G) * st->sm_count;
     SplitPlan plan = plan_decode(units, p.n_stages, capacity);
     p.n_split = plan.n_split;
     p.stages_per_split = plan.stages_per_split;
     p.n_items = units * p.n_split;
-    p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d_h));
+    p.scale_log2 = (float)(1.4426950408889634 * score_temperature(f) / sqrt((double)d_h));
     L.grid = std::min(p.n_items, capacity);
-    if (launch_decode(L, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return APEX_ERR_CUDA;
+    if (launch_decode(L, opt->keys_prerotated != 0, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return APEX_ERR_CUDA;
     return APEX_OK;
 }
 
-apex_status apex_attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
-                          int S_q, int S_k, int d_h, int window, int q_pos0, float rope_base, apex_stream_t stream)
+apex_status apex_attn_decode(const void *q, const void *k_cache, const void *v_cache, void *out, int B, int H_q,
+                             int H_kv, int S_k, int d_h, int window, int q_pos, float rope_base, void *workspace,
+                             size_t workspace_bytes, apex_stream_t stream)
 {
-    if (!q || !k || !v || !out) return APEX_ERR_INVALID_ARG;
+    if (!(rope_base > 0.f)) return APEX_ERR_INVALID_ARG;
+    apex_attn_options o;
+    memset(&o, 0, sizeof o);
+    o.window = window;
+    o.q_pos = q_pos;
+    o.rope_base = rope_base;
+    return apex_attn_decode_ex(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, &o, workspace, workspace_bytes,
+                               stream);
+}
+
+apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
+                             int S_q, int S_k, int d_h, const apex_attn_options *opt, apex_stream_t stream)
+{
+    if (!q || !k || !v || !out || !opt) return APEX_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return APEX_ERR_INVALID_ARG;
-    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, rope_base);
+    RopeFreq f;
+    if (!freq_of(*opt, &f)) return APEX_ERR_INVALID_ARG;
+    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, f.base);
     if (s != APEX_OK) return s;
+    const int q_pos0 = opt->q_pos, window = opt->window, P = opt->prefix_len;
     if (S_q <= 0 || q_pos0 < 0 || (long long)q_pos0 + S_q > (long long)S_k) return APEX_ERR_INVALID_ARG;
+    if (P < 0 || P > S_k) return APEX_ERR_INVALID_ARG;
 
     int dev;
     DeviceState *st = current_state(&dev);
@@ -336,7 +408,7 @@ apex_status apex_attn_fwd(const void *q, const void *k, const void *v, void *out
     s = init_device(*st, dev);
     if (s != APEX_OK) return s;
     RopeTableView tv;
-    s = get_table(*st, d_h, rope_base, S_k, &tv);
+    s = get_table(*st, d_h, f, S_k, &tv);
     if (s != APEX_OK) return s;
 
     const int G = H_q / H_kv;
@@ -359,12 +431,64 @@ apex_status apex_attn_fwd(const void *q, const void *k, const void *v, void *out
     p.d_h = d_h;
     p.window = window > 0 ? window : 0;
     p.q_pos0 = q_pos0;
+    p.prefix_len = P;
+    p.keys_prerotated = opt->keys_prerotated != 0;
     p.rows_per_head = rows_per_head;
     p.n_qblocks = (S_q + 2 * rows_per_head - 1) / (2 * rows_per_head);
     p.n_work = B * H_kv * p.n_qblocks;
-    p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d_h));
+    p.scale_log2 = (float)(1.4426950408889634 * score_temperature(f) / sqrt((double)d_h));
     L.grid = std::min(p.n_work, st->sm_count);
     if (launch_prefill(L, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return APEX_ERR_CUDA;
+    return APEX_OK;
+}
+
+apex_status apex_attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
+                          int S_q, int S_k, int d_h, int window, int q_pos0, float rope_base, apex_stream_t stream)
+{
+    if (!(rope_base > 0.f)) return APEX_ERR_INVALID_ARG;
+    apex_attn_options o;
+    memset(&o, 0, sizeof o);
+    o.window = window;
+    o.q_pos = q_pos0;
+    o.rope_base = rope_base;
+    return apex_attn_fwd_ex(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, &o, stream);
+}
+
+apex_status apex_attn_rope_keys(const void *k_in, void *k_out, int n_heads, int n_pos, int d_h, int pos0,
+                                long long in_head_stride, long long out_head_stride,
+                                const apex_attn_options *opt, apex_stream_t stream)
+{
+    if (!k_in || !k_out || !opt) return APEX_ERR_INVALID_ARG;
+    if (!aligned16(k_in) || !aligned16(k_out)) return APEX_ERR_INVALID_ARG;
+    if (n_heads <= 0 || n_pos <= 0 || pos0 < 0) return APEX_ERR_INVALID_ARG;
+    if (d_h != 64 && d_h != 128) return APEX_ERR_UNSUPPORTED;
+    if (in_head_stride < (long long)n_pos * d_h || out_head_stride < (long long)n_pos * d_h ||
+        (in_head_stride % 8) != 0 || (out_head_stride % 8) != 0)
+        return APEX_ERR_INVALID_ARG;
+    if ((long long)pos0 + n_pos > kMaxSeq) return APEX_ERR_UNSUPPORTED;
+    RopeFreq f;
+    if (!freq_of(*opt, &f)) return APEX_ERR_INVALID_ARG;
+    int dev;
+    DeviceState *st = current_state(&dev);
+    if (!st) return APEX_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(st->mu);
+    apex_status s = init_device(*st, dev);
+    if (s != APEX_OK) return s;
+    RopeTableView tv;
+    s = get_table(*st, d_h, f, pos0 + n_pos, &tv);
+    if (s != APEX_OK) return s;
+    RopeKeysParams p;
+    p.in = static_cast<const uint16_t *>(k_in);
+    p.out = static_cast<uint16_t *>(k_out);
+    p.in_stride = in_head_stride;
+    p.out_stride = out_head_stride;
+    p.n_heads = n_heads;
+    p.n_pos = n_pos;
+    p.d_h = d_h;
+    p.pos0 = pos0;
+    p.rope = tv;
+    if (launch_rope_keys(p, st->sm_count, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return APEX_ERR_CUDA;
     return APEX_OK;
 }
 

@@ -53,7 +53,9 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <int D, int NT>
+// PREROT: the cached keys already hold RoPE(k_j, j); the query is rotated to
+// its absolute position and the keys are used as they are.
+template <int D, int NT, bool PREROT>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const DecodeParams p)
@@ -123,15 +125,20 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int bx = 0; bx < C::kBoxes; ++bx)
                         tma_load_3d(vdst + bx * kBoxBytes, &tm_v, bar_full + 8 * slot, 64 * bx, j0, unit);
                 }
-                // Q' = R(q_pos - j0) q  (Part 1, §4.2 rotation of each interleaved pair)
-                const float2 *cs = p.rope.cs + (size_t)(p.q_pos - j0) * kPairs;
+                // Q' = R(q_pos - j0) q (Part 1, §4.2 rotation of each interleaved pair);
+                // a query inside a prefix can see keys after it: R(-a) = (cos a, -sin a).
+                // With pre-rotated keys, Q' = R(q_pos) q.
+                const int delta = PREROT ? p.q_pos : p.q_pos - j0;
+                const float2 *cs = p.rope.cs + (size_t)(delta < 0 ? -delta : delta) * kPairs;
+                const float sgn = delta < 0 ? -1.f : 1.f;
                 uint8_t *qp = smem + slot * C::kStageBytes + 2 * C::kKBytes;
 #pragma unroll
                 for (int k = 0; k < kPPL; ++k) {
                     const int pi = lane + 32 * k;
                     if (pi < n_pairs) {
                         const int qi = pi / kPairs, i = pi % kPairs;
-                        const float2 c = __ldg(cs + i);
+                        const float2 c0 = __ldg(cs + i);
+                        const float2 c = make_float2(c0.x, sgn * c0.y);
                         const float y0 = fmaf(qv[k].x, c.x, -qv[k].y * c.y);
                         const float y1 = fmaf(qv[k].x, c.y, qv[k].y * c.x);
                         *reinterpret_cast<uint32_t *>(qp + qi * C::kQpRow + 4 * i) = pack_bf16x2(y0, y1);
@@ -213,20 +220,22 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const uint32_t chunk = 2 * s + (lane >> 4);
                     uint32_t a[4];
                     ldmatrix_x4(a, kb + (chunk >> 3) * kBoxBytes + swz128(row, chunk & 7));
-                    a[0] = rope_pair_bf16(a[0], csk[0][2 * s].x, csk[0][2 * s].y);
-                    a[1] = rope_pair_bf16(a[1], csk[1][2 * s].x, csk[1][2 * s].y);
-                    a[2] = rope_pair_bf16(a[2], csk[0][2 * s + 1].x, csk[0][2 * s + 1].y);
-                    a[3] = rope_pair_bf16(a[3], csk[1][2 * s + 1].x, csk[1][2 * s + 1].y);
+                    if (!PREROT) {
+                        a[0] = rope_pair_bf16(a[0], csk[0][2 * s].x, csk[0][2 * s].y);
+                        a[1] = rope_pair_bf16(a[1], csk[1][2 * s].x, csk[1][2 * s].y);
+                        a[2] = rope_pair_bf16(a[2], csk[0][2 * s + 1].x, csk[0][2 * s + 1].y);
+                        a[3] = rope_pair_bf16(a[3], csk[1][2 * s + 1].x, csk[1][2 * s + 1].y);
+                    }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc_s[nt], a, bq[nt][2 * h2], bq[nt][2 * h2 + 1]);
                 }
             }
 
             // online softmax over this warp's 16 keys (log2 units)
-            const bool edge = (j0 < p.k_lo) || (j0 + kKeys - 1 > p.q_pos);
+            const bool edge = (j0 < p.k_lo) || (j0 + kKeys - 1 > p.k_hi);
             const int key0 = j0 + 16 * warp + g, key1 = key0 + 8;
-            const bool ok0 = !edge || (key0 >= p.k_lo && key0 <= p.q_pos);
-            const bool ok1 = !edge || (key1 >= p.k_lo && key1 <= p.q_pos);
+            const bool ok0 = !edge || (key0 >= p.k_lo && key0 <= p.k_hi);
+            const bool ok1 = !edge || (key1 >= p.k_lo && key1 <= p.k_hi);
             uint32_t bp[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -356,14 +365,14 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
     for (int e = 0; e < E / 2; ++e) dst[e] = packed[e];
 }
 
-template <int D, int NT>
+template <int D, int NT, bool PREROT>
 cudaError_t launch_t(const DecodeLaunch &L, cudaStream_t stream)
 {
     using C = DecodeCfg<D, NT>;
-    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           C::kSmemBytes);
+    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<D, NT, PREROT>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
-    decode_split_kernel<D, NT><<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tm_k, L.tm_v, L.p);
+    decode_split_kernel<D, NT, PREROT><<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tm_k, L.tm_v, L.p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const int rows = L.p.B * L.p.H_q;
@@ -371,14 +380,20 @@ cudaError_t launch_t(const DecodeLaunch &L, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-}  // namespace
-
-cudaError_t launch_decode(const DecodeLaunch &L, cudaStream_t stream)
+template <bool PREROT>
+cudaError_t dispatch(const DecodeLaunch &L, cudaStream_t stream)
 {
     const bool wide = L.p.G > 8;
-    if (L.p.d_h == 128) return wide ? launch_t<128, 2>(L, stream) : launch_t<128, 1>(L, stream);
-    if (L.p.d_h == 64) return wide ? launch_t<64, 2>(L, stream) : launch_t<64, 1>(L, stream);
+    if (L.p.d_h == 128) return wide ? launch_t<128, 2, PREROT>(L, stream) : launch_t<128, 1, PREROT>(L, stream);
+    if (L.p.d_h == 64) return wide ? launch_t<64, 2, PREROT>(L, stream) : launch_t<64, 1, PREROT>(L, stream);
     return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeLaunch &L, bool keys_prerotated, cudaStream_t stream)
+{
+    return keys_prerotated ? dispatch<true>(L, stream) : dispatch<false>(L, stream);
 }
 
 int decode_ctas_per_sm(int d_h, int G)

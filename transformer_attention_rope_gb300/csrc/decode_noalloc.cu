@@ -169,6 +169,7 @@ extern "C" apex_status apex_attn_decode_noalloc(const void *q, const void *k_cac
     p.d_h = d_h;
     p.q_pos = q_pos;
     p.k_lo = (window > 0) ? std::max(0, q_pos - window + 1) : 0;
+    p.k_hi = q_pos;
     p.stage0 = p.k_lo / kDecodeKeysPerStage;
     p.n_stages = q_pos / kDecodeKeysPerStage - p.stage0 + 1;
 
@@ -198,6 +199,6 @@ extern "C" apex_status apex_attn_decode_noalloc(const void *q, const void *k_cac
     p.ws_ml = reinterpret_cast<float2 *>(st.scratch + o_bytes);
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d_h));
     L.grid = std::min(p.n_items, capacity);
-    if (launch_decode(L, s) != cudaSuccess) return APEX_ERR_CUDA;
+    if (launch_decode(L, false, s) != cudaSuccess) return APEX_ERR_CUDA;
     return APEX_OK;
 }

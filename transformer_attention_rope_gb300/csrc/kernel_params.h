@@ -37,6 +37,7 @@ struct DecodeParams {
     int B, H_q, H_kv, G, S_k, d_h;
     int q_pos;              // query position
     int k_lo;               // first visible key
+    int k_hi;               // last visible key (q_pos, or P - 1 for a query inside a prefix of P)
     int stage0;             // first stage index (stage s covers keys [64 s, 64 s + 64))
     int n_stages;           // stages per (b, kv-head)
     int n_split;            // splits per (b, kv-head)
@@ -51,7 +52,8 @@ struct DecodeLaunch {
     int grid;                // CTAs of the split kernel (persistent)
 };
 
-cudaError_t launch_decode(const DecodeLaunch &L, cudaStream_t stream);
+// keys_prerotated selects the variant that uses the cached keys as they are
+cudaError_t launch_decode(const DecodeLaunch &L, bool keys_prerotated, cudaStream_t stream);
 int decode_ctas_per_sm(int d_h, int G);
 
 // ----------------------------------------------------------------- prefill
@@ -62,6 +64,8 @@ struct PrefillParams {
     int B, H_q, H_kv, G, S_q, S_k, d_h;
     int window;     // <= 0: none
     int q_pos0;
+    int prefix_len;       // bidirectional prefix [0, P); 0: none
+    int keys_prerotated;  // keys already rotated: no K RoPE
     int rows_per_head;   // query positions per head in one 128-row M tile (128 / G)
     int n_qblocks;       // position blocks per (b, kv-head); a block = 2 M tiles
     int n_work;          // B * H_kv * n_qblocks (work items, walked by a persistent grid)
@@ -75,5 +79,16 @@ struct PrefillLaunch {
 };
 
 cudaError_t launch_prefill(const PrefillLaunch &L, cudaStream_t stream);
+
+// ----------------------------------------------------------------- key rotation
+struct RopeKeysParams {
+    const uint16_t *in;
+    uint16_t *out;
+    long long in_stride, out_stride;  // elements between heads
+    int n_heads, n_pos, d_h, pos0;
+    RopeTableView rope;
+};
+
+cudaError_t launch_rope_keys(const RopeKeysParams &p, int sm_count, cudaStream_t stream);
 
 }  // namespace apex

@@ -219,8 +219,12 @@ __device__ __forceinline__ Item make_item(const PrefillParams &p, int w)
     it.r0 = qblock * 2 * P;
     const int rows = min(2 * P, p.S_q - it.r0);
     const int m_first = p.q_pos0 + it.r0, m_last = p.q_pos0 + it.r0 + rows - 1;
-    it.j_lo = (p.window > 0) ? max(0, m_first - p.window + 1) / 128 : 0;
-    it.n_kt = m_last / 128 - it.j_lo + 1;
+    // union of the rows' visible key ranges: [lo(m), m] (Part 2, §10.2), or the
+    // whole prefix [0, P) for rows inside it (§11.1)
+    const int key_lo = (m_first < p.prefix_len || p.window <= 0) ? 0 : max(0, m_first - p.window + 1);
+    const int key_hi = (m_first < p.prefix_len) ? max(m_last, p.prefix_len - 1) : m_last;
+    it.j_lo = key_lo / 128;
+    it.n_kt = key_hi / 128 - it.j_lo + 1;
     it.zq = it.b * p.H_q + it.hk * p.G;
     return it;
 }
@@ -392,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < it.n_kt; ++j, ++kc) {
                 const int ks = kc % kKStages;
                 mbar_wait(bar(C::kBarKFull + ks), (kc / kKStages) & 1, p.wait);
-                kr.rotate(smem + C::kKOff + ks * C::kTile, rt);
+                if (!p.keys_prerotated) kr.rotate(smem + C::kKOff + ks * C::kTile, rt);
                 if (j + 1 < it.n_kt) kr.load_seed(p.rope.cs, min(128 * (it.j_lo + j + 1) + r0, max_row), c);
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -423,17 +427,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Item it = make_item(p, w);
             const int r = it.r0 + t * P + i % P;  // query row index
             const int m = p.q_pos0 + r;           // its position
+            // keys this row sees: [key_lo, key_hi]
+            const bool in_prefix = m < p.prefix_len;
+            const int key_lo = (in_prefix || W <= 0) ? 0 : m - W + 1;
+            const int key_hi = in_prefix ? p.prefix_len - 1 : m;
             float m_run = -INFINITY, l_run = 0.f;
 
             for (int j = 0; j < it.n_kt; ++j) {
                 mbar_wait(bar(C::kBarSFull + t), (kc + j) & 1, p.wait);
                 tc_fence_after();
                 const int kstart = 128 * (it.j_lo + j);
-                const bool full_vis = (kstart + 127 <= m) && (W == 0 || m - kstart < W);
+                // columns [lo_c, hi_c] of this tile are visible to the row
+                const int hi_c = key_hi - kstart;
+                const int lo_c = key_lo - kstart;
+                const bool full_vis = lo_c <= 0 && hi_c >= 127;
                 const bool all_full = __all_sync(0xffffffffu, full_vis);
-                // columns [lo_c, hi_c] of this tile are visible to the row (Part 2, §10.2)
-                const int hi_c = m - kstart;
-                const int lo_c = (W > 0) ? m - W + 1 - kstart : -1000000;
                 // the whole 128-column row of S in registers
                 uint32_t v[128];
 #pragma unroll

@@ -45,24 +45,40 @@ PREFILL = "gqa"
 DECODE = "decode"
 
 
-def visible_pairs(S_q, S_k, window, q_pos0):
-    """Number of (query, key) pairs the causal/window mask leaves visible, per head."""
+def visible_range(m, window, prefix_len=0):
+    """Keys [lo, hi] a query at position m sees (causal/window; a whole prefix inside it)."""
+    if m < prefix_len:
+        return 0, prefix_len - 1
+    return (max(0, m - window + 1) if window > 0 else 0), m
+
+
+def visible_pairs(S_q, S_k, window, q_pos0, prefix_len=0):
+    """Number of (query, key) pairs the mask leaves visible, per head."""
     total = 0
     for r in range(S_q):
-        m = q_pos0 + r
-        lo = max(0, m - window + 1) if window > 0 else 0
-        total += min(m, S_k - 1) - lo + 1
+        lo, hi = visible_range(q_pos0 + r, window, prefix_len)
+        total += min(hi, S_k - 1) - lo + 1
     return total
 
 
-def prefill_flops(w):
-    return 4.0 * w.d_h * visible_pairs(w.S_q, w.S_k, w.window, w.q_pos0) * w.B * w.H_q
+def prefill_flops(w, prefix_len=0):
+    return 4.0 * w.d_h * visible_pairs(w.S_q, w.S_k, w.window, w.q_pos0, prefix_len) * w.B * w.H_q
 
 
-def decode_kv_bytes(w):
-    m = w.q_pos0
-    lo = max(0, m - w.window + 1) if w.window > 0 else 0
-    return 2.0 * w.B * w.H_kv * (m - lo + 1) * w.d_h * 2
+def decode_kv_bytes(w, prefix_len=0):
+    lo, hi = visible_range(w.q_pos0, w.window, prefix_len)
+    return 2.0 * w.B * w.H_kv * (hi - lo + 1) * w.d_h * 2
+
+
+# --feature: the options of the block beyond the plain path, as keyword arguments
+# of apex.fwd / apex.decode (YaRN with the pages' s = 32; a 1024-position
+# bidirectional prefix; keys pre-rotated once before timing)
+FEATURES = {
+    "none": {},
+    "yarn": {"yarn_scale": 32.0},
+    "prefix": {"prefix_len": 1024},
+    "prerotated": {"keys_prerotated": True},
+}
 
 
 def rank_workloads(rank, prefill_name=PREFILL, decode_batch=None):
@@ -298,11 +314,21 @@ def run_ours(args):
         apex.apex_attn_rope_reserve(wd.S_k, wd.d_h, wd.rope_base)
     torch.cuda.synchronize()
 
+    feat = FEATURES[args.feature]
+    if feat.get("keys_prerotated"):
+        # the caches hold RoPE(k_j, j): rotate the keys once, outside the timing
+        if do_pre:
+            pk = apex.rope_keys(pk)
+        if do_dec:
+            dk = apex.rope_keys(dk)
+        torch.cuda.synchronize()
+
     def prefill():
-        apex.fwd(pq, pk, pv, window=wp.window, q_pos0=wp.q_pos0, rope_base=wp.rope_base, out=pout)
+        apex.fwd(pq, pk, pv, window=wp.window, q_pos0=wp.q_pos0, rope_base=wp.rope_base, out=pout, **feat)
 
     def decode():
-        apex.decode(dq, dk, dv, wd.q_pos0, window=wd.window, rope_base=wd.rope_base, out=dout, workspace=ws)
+        apex.decode(dq, dk, dv, wd.q_pos0, window=wd.window, rope_base=wd.rope_base, out=dout, workspace=ws,
+                    **feat)
 
     warm = max(3, args.warmup)
     for _ in range(warm):
@@ -344,6 +370,8 @@ def run_ours(args):
 
     # ---- end to end through the C ABI with pinned host buffers
     h2d = sum(t.numel() * t.element_size() for t in (*pin, *din))
+    if feat.get("keys_prerotated"):  # the pre-rotated key caches stay on the device
+        h2d -= sum(t.numel() * t.element_size() for t in (pin[1:2] + din[1:2]))
     d2h = (pout.numel() * 2 if do_pre else 0) + (dout.numel() * 2 if do_dec else 0)
     evx = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     if pg:
@@ -353,13 +381,15 @@ def run_ours(args):
         evx[i][0].record(stream)
         if do_pre:
             for dst, src in zip((pq, pk, pv), pin):
-                dst.copy_(src, non_blocking=True)
+                if not (feat.get("keys_prerotated") and src is pin[1]):
+                    dst.copy_(src, non_blocking=True)
             prefill()
             pout_h.copy_(pout, non_blocking=True)
         evx[i][1].record(stream)
         if do_dec:
             for dst, src in zip((dq, dk, dv), din):
-                dst.copy_(src, non_blocking=True)
+                if not (feat.get("keys_prerotated") and src is din[1]):
+                    dst.copy_(src, non_blocking=True)
             decode()
             dout_h.copy_(dout, non_blocking=True)
         evx[i][2].record(stream)
@@ -367,12 +397,12 @@ def run_ours(args):
     te_pre = sum(e[0].elapsed_time(e[1]) for e in evx) / 1e3
     te_dec = sum(e[1].elapsed_time(e[2]) for e in evx) / 1e3
 
-    flops = prefill_flops(wp)
-    kvb = decode_kv_bytes(wd)
+    flops = prefill_flops(wp, feat.get("prefix_len", 0))
+    kvb = decode_kv_bytes(wd, feat.get("prefix_len", 0))
     t_pre, t_dec, t_all, te_pre, te_dec = max_over_ranks([t_pre, t_dec, t_all, te_pre, te_dec], pg, dev)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and do_pre and do_dec:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and do_pre and do_dec and args.feature == "none":
         cpu = cpu_baseline(wp, wd, pin, din)
 
     if rank == 0:
@@ -388,6 +418,8 @@ def run_ours(args):
         if do_dec:
             desc.append("decode (B%d Hq%d Hkv%d Sk%d d%d q_pos %d)" % (wd.B, wd.H_q, wd.H_kv, wd.S_k, wd.d_h,
                                                                         wd.q_pos0))
+        if args.feature != "none":
+            desc.append("feature %s %s" % (args.feature, json.dumps(feat)))
         line["config"] = {
             "workload": " + ".join(desc),
             "l2": "inputs larger than L2 (prefill Q+K+V >= 201 MB; decode K+V 8.6 GB streamed every step)",
@@ -475,6 +507,8 @@ def main():
     ap.add_argument("--part", choices=["all", "prefill", "decode"], default="all",
                     help="run only one of the two calls per step (profiling)")
     ap.add_argument("--prefill-workload", choices=["tiny", "gqa", "wide", "long"], default=PREFILL)
+    ap.add_argument("--feature", choices=sorted(FEATURES), default="none",
+                    help="run the step with one of the block's options")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="decode batch size (profiling a smaller case; default: the workload's 64)")
     args = ap.parse_args()

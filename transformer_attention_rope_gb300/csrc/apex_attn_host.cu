@@ -57,6 +57,15 @@ uint64_t wait_timeout_ns()
     return v;
 }
 
+// Prefill kernel choice for the plain block: APEX_ATTN_PREFILL=pair (read at
+// each call) selects the CTA-pair kernel (d_h = 128 only), anything else the
+// single-CTA kernel.
+bool use_pair_prefill(int d_h, int sm_count)
+{
+    const char *e = getenv("APEX_ATTN_PREFILL");
+    return e && strcmp(e, "pair") == 0 && d_h == 128 && sm_count >= 2;
+}
+
 apex_status init_device(DeviceState &st, int dev)
 {
     if (st.ready) return APEX_OK;
@@ -413,10 +422,12 @@ apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *
 
     const int G = H_q / H_kv;
     const int rows_per_head = 128 / G;
+    const bool pair = use_pair_prefill(d_h, st->sm_count);
     PrefillLaunch L;
     memset(&L, 0, sizeof L);
     if (!make_map(&L.tm_q, q, d_h, S_q, B * H_q, rows_per_head, G) ||
-        !make_map(&L.tm_k, k, d_h, S_k, B * H_kv, 128, 1) || !make_map(&L.tm_v, v, d_h, S_k, B * H_kv, 128, 1))
+        !make_map(&L.tm_k, k, d_h, S_k, B * H_kv, pair ? 64 : 128, 1) ||
+        !make_map(&L.tm_v, v, d_h, S_k, B * H_kv, 128, 1))
         return APEX_ERR_CUDA;
     PrefillParams &p = L.p;
     p.out = static_cast<uint16_t *>(out);
@@ -434,11 +445,17 @@ apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *
     p.prefix_len = P;
     p.keys_prerotated = opt->keys_prerotated != 0;
     p.rows_per_head = rows_per_head;
-    p.n_qblocks = (S_q + 2 * rows_per_head - 1) / (2 * rows_per_head);
+    const int block_rows = (pair ? 4 : 2) * rows_per_head;
+    p.n_qblocks = (S_q + block_rows - 1) / block_rows;
     p.n_work = B * H_kv * p.n_qblocks;
     p.scale_log2 = (float)(1.4426950408889634 * score_temperature(f) / sqrt((double)d_h));
-    L.grid = std::min(p.n_work, st->sm_count);
-    if (launch_prefill(L, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return APEX_ERR_CUDA;
+    if (pair) {
+        L.grid = 2 * std::min(p.n_work, st->sm_count / 2);
+        if (launch_prefill_pair(L, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return APEX_ERR_CUDA;
+    } else {
+        L.grid = std::min(p.n_work, st->sm_count);
+        if (launch_prefill(L, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return APEX_ERR_CUDA;
+    }
     return APEX_OK;
 }
 

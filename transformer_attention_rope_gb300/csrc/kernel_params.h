@@ -67,7 +67,7 @@ struct PrefillParams {
     int prefix_len;       // bidirectional prefix [0, P); 0: none
     int keys_prerotated;  // keys already rotated: no K RoPE
     int rows_per_head;   // query positions per head in one 128-row M tile (128 / G)
-    int n_qblocks;       // position blocks per (b, kv-head); a block = 2 M tiles
+    int n_qblocks;       // position blocks per (b, kv-head); a block = 2 M tiles (4 on CTA pairs)
     int n_work;          // B * H_kv * n_qblocks (work items, walked by a persistent grid)
     float scale_log2;    // log2(e) / sqrt(d_h)
 };
@@ -79,6 +79,8 @@ struct PrefillLaunch {
 };
 
 cudaError_t launch_prefill(const PrefillLaunch &L, cudaStream_t stream);
+// CTA-pair variant (d_h = 128): tm_k's box is {64, 64, 1}, grid even, blocks of 4 M tiles
+cudaError_t launch_prefill_pair(const PrefillLaunch &L, cudaStream_t stream);
 
 // ----------------------------------------------------------------- key rotation
 struct RopeKeysParams {

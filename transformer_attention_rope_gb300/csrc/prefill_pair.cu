@@ -1,0 +1,649 @@
+// prefill_pair.cu -- the prefill on CTA pairs (tcgen05 cta_group::2), d_h = 128.
+//
+// Same computation as prefill.cu (RoPE on Q and K tiles in shared memory, GQA
+// packing of the G heads that share a KV head into each 128-row M tile, online
+// exp2 softmax, key tiles outside the causal/window/prefix bounds skipped), but
+// a work item is four M tiles of one (batch, kv head) unit spread over the two
+// CTAs of a cluster, and each 128-key tile is shared by both CTAs:
+//
+//   * S_t = Q_t K^T and O_t += P_t V run as M = 256 MMAs issued by the leader
+//     CTA (rank 0): rows 0-127 are the leader's tile t, rows 128-255 the
+//     peer's; the B operand is split along N between the two shared memories,
+//     so each CTA loads -- and rotates -- only 64 of the 128 keys of every K
+//     tile, and holds only 64 of the 128 dims of every V tile.
+//   * TMEM is allocated for the pair; each CTA's softmax warpgroups read their
+//     own S rows and write their own P and O rows, as in the single-CTA kernel.
+//   * The leader's MMA thread waits on its own barriers, which the peer's warps
+//     reach through remote (shared::cluster) arrivals; its commits are
+//     multicast, so every CTA waits on local barriers only.
+//
+// Warps per CTA: 0-3 / 4-7 softmax + epilogue of tiles 0 / 1 (and their Q
+// RoPE), 8-11 K RoPE, 12 TMA producer, 13 MMA issuer (leader) / TMEM
+// allocation, 14 relays "V landed" to the leader, 15 idle.
+#include <math.h>
+
+#include "device_common.cuh"
+#include "tcgen05.cuh"
+
+namespace apex {
+namespace {
+
+constexpr int D = 128;
+constexpr int kThreads = 16 * 32;
+constexpr int kWarpRope = 8;
+constexpr int kWarpTma = 12;
+constexpr int kWarpMma = 13;
+constexpr int kWarpRelay = 14;
+constexpr int kKStages = 4;
+constexpr int kVStages = 4;
+constexpr int kLaunchRegs = 128;
+constexpr int kRegsSoftmax = 168;
+constexpr int kRegsRope = 88;
+constexpr int kRegsCtl = 88;
+static_assert(128 * (2 * kRegsSoftmax + kRegsRope + kRegsCtl) <= kThreads * kLaunchRegs, "register split");
+
+constexpr int kQBox = 128 * 128;                 // [128 rows][64 dims]
+constexpr int kQTile = 2 * kQBox;                // 128 x 128
+constexpr int kKBox = 64 * 128;                  // [64 keys][64 dims]
+constexpr int kKTile = 2 * kKBox;                // this CTA's 64 keys x 128 dims
+constexpr int kVTile = 128 * 128;                // 128 keys x this CTA's 64 dims
+// Q | V stages | K stages | 8 KB guard | barriers: an operand descriptor that
+// walked past its tile (it should not: each CTA's B half is 64 rows or 64
+// columns) would still stay inside the allocation.
+constexpr int kQOff = 0;
+constexpr int kVOff = 2 * kQTile;
+constexpr int kKOff = kVOff + kVStages * kVTile;
+constexpr int kBarOff = kKOff + kKStages * kKTile + 8192;
+
+// barrier slots
+constexpr int kBarQFull = 0;                         // [2]  local TMA
+constexpr int kBarQReady = 2;                        // [2]  leader: 8 warps (both CTAs)
+constexpr int kBarQEmpty = 4;                        // [2]  multicast commit
+constexpr int kBarSFull = 6;                         // [2]  multicast commit
+constexpr int kBarPReady = 8;                        // [2]  leader: 8 warps
+constexpr int kBarODone = 10;                        // [2]  multicast commit
+constexpr int kBarKFull = 12;                        // [K]  local TMA
+constexpr int kBarKReady = kBarKFull + kKStages;     // [K]  leader: 8 warps
+constexpr int kBarKEmpty = kBarKReady + kKStages;    // [K]  multicast commit
+constexpr int kBarVFull = kBarKEmpty + kKStages;     // [V]  local TMA
+constexpr int kBarVReady = kBarVFull + kVStages;     // [V]  leader: 2 relays
+constexpr int kBarVEmpty = kBarVReady + kVStages;    // [V]  multicast commit
+constexpr int kNumBars = kBarVEmpty + kVStages;
+constexpr int kTmemSlot = kBarOff + kNumBars * 8;
+constexpr int kSmemBytes = kTmemSlot + 16 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+
+__device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
+__device__ __forceinline__ uint32_t col_o(int t) { return 256u + 128u * t; }
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p)
+{
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// ---------------------------------------------------------------- cluster helpers
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on the barrier at the same shared-memory offset in the leader CTA.
+// Default (release, CTA-scope) semantics: a cluster-scope release here costs
+// about a microsecond per arrival on the softmax critical path.
+__device__ __forceinline__ void arrive_leader(uint32_t local_bar)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_bar), "r"(0));
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+// Bounded wait on a local barrier (some receive arrivals from the peer CTA).
+// On time-out the status word and the CTA's abort flag (shared memory) are
+// set and the wait returns; once the flag is set, later waits of the CTA that
+// do not complete at once give up at their first timer check, so a broken
+// pipeline drains in about one time-out.
+__device__ __forceinline__ void pair_wait(uint32_t bar, uint32_t parity, const WaitCtl &wc, volatile uint32_t *abort)
+{
+    if (mbar_try_wait(bar, parity)) return;
+    uint64_t t0 = 0;
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return;
+        if ((n & 255u) == 0) {
+            if (*abort) return;
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > wc.timeout_ns) {
+                *abort = 1u;
+                report_status(wc.status, kStatusWaitTimeout);
+                return;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void commit_pair(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                     bar),
+                 "h"((uint16_t)3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// ---------------------------------------------------------------- RoPE in shared memory
+// A 16-byte chunk holds 4 interleaved pairs (Part 1, §4.2): chunk c of box bx
+// holds pairs 32 bx + 4 c + e, e < 4.  (x_2i, x_2i+1) -> (x c - y s, x s + y c)
+// in fp32 on packed pairs, rounded to bf16.
+__device__ __forceinline__ uint4 rope_chunk(uint4 v, const uint64_t (&C)[2], const uint64_t (&S)[2])
+{
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t w0 = w[2 * h], w1 = w[2 * h + 1];
+        const uint64_t X = f2_pack(bf16lo_to_f32(w0), bf16lo_to_f32(w1));
+        const uint64_t Y = f2_pack(bf16hi_to_f32(w0), bf16hi_to_f32(w1));
+        const uint64_t Xn = f2_fma(Y, f2_neg(S[h]), f2_mul(X, C[h]));
+        const uint64_t Yn = f2_fma(X, S[h], f2_mul(Y, C[h]));
+        float x0, x1, y0, y1;
+        f2_unpack(Xn, x0, x1);
+        f2_unpack(Yn, y0, y1);
+        w[2 * h] = pack_bf16x2(x0, y0);
+        w[2 * h + 1] = pack_bf16x2(x1, y1);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// This CTA's half of a K tile: 64 key rows (position pos0 + r), stored as two
+// [64 rows][64 dims] swizzled boxes.  Thread rt owns chunk c = rt & 7 of rows
+// r0 + 16 k (r0 = rt >> 3, k < 4); the angle advances by 16 positions per
+// step: z_{k+1} = z_k * (cos 16 theta, sin 16 theta), seeded per tile.
+struct KHalfRope {
+    uint64_t WC[2][2], WS[2][2];
+    float4 seed[2][2];
+
+    __device__ __forceinline__ void init(const float2 *table, int c)
+    {
+#pragma unroll
+        for (int bx = 0; bx < 2; ++bx) {
+            const float4 *p = reinterpret_cast<const float4 *>(table + 16 * (D / 2) + 32 * bx + 4 * c);
+            const float4 a = __ldg(p), b = __ldg(p + 1);
+            WC[bx][0] = f2_pack(a.x, a.z);
+            WS[bx][0] = f2_pack(a.y, a.w);
+            WC[bx][1] = f2_pack(b.x, b.z);
+            WS[bx][1] = f2_pack(b.y, b.w);
+        }
+    }
+    __device__ __forceinline__ void load_seed(const float2 *table, int pos, int c)
+    {
+#pragma unroll
+        for (int bx = 0; bx < 2; ++bx) {
+            const float4 *p = reinterpret_cast<const float4 *>(table + (size_t)pos * (D / 2) + 32 * bx + 4 * c);
+            seed[bx][0] = __ldg(p);
+            seed[bx][1] = __ldg(p + 1);
+        }
+    }
+    __device__ __forceinline__ void rotate(uint8_t *tile, int rt)
+    {
+        const int c = rt & 7, r0 = rt >> 3;
+        uint64_t C[2][2], S[2][2];
+#pragma unroll
+        for (int bx = 0; bx < 2; ++bx) {
+            C[bx][0] = f2_pack(seed[bx][0].x, seed[bx][0].z);
+            S[bx][0] = f2_pack(seed[bx][0].y, seed[bx][0].w);
+            C[bx][1] = f2_pack(seed[bx][1].x, seed[bx][1].z);
+            S[bx][1] = f2_pack(seed[bx][1].y, seed[bx][1].w);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int row = r0 + 16 * k;
+#pragma unroll
+            for (int bx = 0; bx < 2; ++bx) {
+                uint4 *ptr = reinterpret_cast<uint4 *>(tile + bx * kKBox + swz128(row, c));
+                *ptr = rope_chunk(*ptr, C[bx], S[bx]);
+                if (k < 3) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t Cn = f2_fma(C[bx][h], WC[bx][h], f2_mul(S[bx][h], f2_neg(WS[bx][h])));
+                        const uint64_t Sn = f2_fma(C[bx][h], WS[bx][h], f2_mul(S[bx][h], WC[bx][h]));
+                        C[bx][h] = Cn;
+                        S[bx][h] = Sn;
+                    }
+                }
+            }
+        }
+    }
+};
+
+// Q tile: head-major rows (row = head * P + p); all G heads of position p share
+// one set of angles.  Thread rt takes the (p, chunk) combos rt, rt + 128, ...
+__device__ __forceinline__ void rope_q_tile(uint8_t *tile, int rt, const float2 *table, int pos0, int G, int P,
+                                            int valid_p)
+{
+    for (int q = rt; q < P * 8; q += 128) {
+        const int pp = q >> 3, c = q & 7;
+        if (pp >= valid_p) continue;
+        uint64_t C[2][2], S[2][2];
+#pragma unroll
+        for (int bx = 0; bx < 2; ++bx) {
+            const float4 *t = reinterpret_cast<const float4 *>(table + (size_t)(pos0 + pp) * (D / 2) + 32 * bx + 4 * c);
+            const float4 a = __ldg(t), b = __ldg(t + 1);
+            C[bx][0] = f2_pack(a.x, a.z);
+            S[bx][0] = f2_pack(a.y, a.w);
+            C[bx][1] = f2_pack(b.x, b.z);
+            S[bx][1] = f2_pack(b.y, b.w);
+        }
+        for (int hl = 0; hl < G; ++hl) {
+            const int row = hl * P + pp;
+#pragma unroll
+            for (int bx = 0; bx < 2; ++bx) {
+                uint4 *ptr = reinterpret_cast<uint4 *>(tile + bx * kQBox + swz128(row, c));
+                *ptr = rope_chunk(*ptr, C[bx], S[bx]);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- work items
+// One item: a (batch, kv head) unit and a block of 4P query rows (P = 128 / G):
+// tile T = 2 rank + t of the pair covers rows r0 + T P .. r0 + T P + P - 1.
+struct Item {
+    int unit, r0, j_lo, n_kt, zq;
+};
+
+__device__ __forceinline__ Item make_item(const PrefillParams &p, int w)
+{
+    Item it;
+    const int units = p.B * p.H_kv;
+    const int qblock = p.n_qblocks - 1 - w / units;  // latest positions (most key tiles) first
+    it.unit = w % units;
+    const int b = it.unit / p.H_kv, hk = it.unit % p.H_kv;
+    const int P = p.rows_per_head;
+    it.r0 = qblock * 4 * P;
+    const int rows = min(4 * P, p.S_q - it.r0);
+    const int m_first = p.q_pos0 + it.r0, m_last = p.q_pos0 + it.r0 + rows - 1;
+    const int key_lo = (m_first < p.prefix_len || p.window <= 0) ? 0 : max(0, m_first - p.window + 1);
+    const int key_hi = (m_first < p.prefix_len) ? max(m_last, p.prefix_len - 1) : m_last;
+    it.j_lo = key_lo / 128;
+    it.n_kt = key_hi / 128 - it.j_lo + 1;
+    it.zq = b * p.H_q + hk * p.G;
+    return it;
+}
+
+// k-th item of this pair: rounds of n_pairs items, walked in alternating direction.
+__device__ __forceinline__ int item_index(int k)
+{
+    const int g = gridDim.x >> 1, c = blockIdx.x >> 1;
+    return k * g + ((k & 1) ? (g - 1 - c) : c);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    auto bar = [&](int i) -> uint32_t { return sb + kBarOff + 8 * i; };
+    const int P = p.rows_per_head;
+    volatile uint32_t *abort = reinterpret_cast<volatile uint32_t *>(smem + kTmemSlot + 4);
+
+    if (threadIdx.x == 0) {
+        *abort = 0u;
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(kBarQFull + t), 1);
+            mbar_init(bar(kBarQReady + t), 8);
+            mbar_init(bar(kBarQEmpty + t), 1);
+            mbar_init(bar(kBarSFull + t), 1);
+            mbar_init(bar(kBarPReady + t), 8);
+            mbar_init(bar(kBarODone + t), 1);
+        }
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(bar(kBarKFull + s), 1);
+            mbar_init(bar(kBarKReady + s), 8);
+            mbar_init(bar(kBarKEmpty + s), 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(bar(kBarVFull + s), 1);
+            mbar_init(bar(kBarVReady + s), 2);
+            mbar_init(bar(kBarVEmpty + s), 1);
+        }
+        fence_mbarrier_init();
+    }
+    if (warp == kWarpMma) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sb + kTmemSlot),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync();  // both CTAs' barriers initialised, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kTmemSlot);
+
+    if (warp >= kWarpTma) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+    if (warp == kWarpTma) {
+        // ------------------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            int kc = 0;
+            for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
+                const Item it = make_item(p, w);
+                for (int t = 0; t < 2; ++t) {
+                    pair_wait(bar(kBarQEmpty + t), (k & 1) ^ 1, p.wait, abort);
+                    mbar_arrive_expect_tx(bar(kBarQFull + t), kQTile);
+#pragma unroll
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_load_3d(sb + kQOff + t * kQTile + bx * kQBox, &tm_q, bar(kBarQFull + t), 64 * bx,
+                                    it.r0 + (2 * (int)rank + t) * P, it.zq);
+                }
+                for (int j = 0; j < it.n_kt; ++j, ++kc) {
+                    const int key0 = 128 * (it.j_lo + j);
+                    const int ks = kc % kKStages, vs = kc % kVStages;
+                    pair_wait(bar(kBarKEmpty + ks), ((kc / kKStages) & 1) ^ 1, p.wait, abort);
+                    mbar_arrive_expect_tx(bar(kBarKFull + ks), kKTile);
+#pragma unroll
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_load_3d(sb + kKOff + ks * kKTile + bx * kKBox, &tm_k, bar(kBarKFull + ks), 64 * bx,
+                                    key0 + 64 * (int)rank, it.unit);
+                    pair_wait(bar(kBarVEmpty + vs), ((kc / kVStages) & 1) ^ 1, p.wait, abort);
+                    mbar_arrive_expect_tx(bar(kBarVFull + vs), kVTile);
+                    tma_load_3d(sb + kVOff + vs * kVTile, &tm_v, bar(kBarVFull + vs), 64 * (int)rank, key0, it.unit);
+                }
+            }
+        }
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------ MMA issuer (leader)
+        if (rank == 0 && lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(256, 128, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(256, 128, true);
+            auto issue_qk = [&](int t, int ks) {
+                const uint32_t qa = sb + kQOff + t * kQTile;
+                const uint32_t kb = sb + kKOff + ks * kKTile;
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s)
+                    mma_ss_pair(tmem + col_s(t), smem_desc_sw128(qa + (s >> 2) * kQBox + (s & 3) * 32, 16, 1024),
+                                smem_desc_sw128(kb + (s >> 2) * kKBox + (s & 3) * 32, 16, 1024), idesc_qk,
+                                s > 0 ? 1u : 0u);
+            };
+            auto issue_pv = [&](int t, int vs, bool acc) {
+                const uint32_t vb = sb + kVOff + vs * kVTile;
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_ts_pair(tmem + col_o(t), tmem + col_s(t) + 8 * s, smem_desc_sw128(vb + s * 2048, kQBox, 1024),
+                                idesc_pv, (acc || s > 0) ? 1u : 0u);
+            };
+            int kc = 0;
+            for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
+                const Item it = make_item(p, w);
+                const int n = it.n_kt;
+                pair_wait(bar(kBarKReady + kc % kKStages), (kc / kKStages) & 1, p.wait, abort);
+                for (int t = 0; t < 2; ++t) {
+                    pair_wait(bar(kBarQReady + t), k & 1, p.wait, abort);
+                    tc_fence_after();
+                    issue_qk(t, kc % kKStages);
+                    commit_pair(bar(kBarSFull + t));
+                    if (n == 1) commit_pair(bar(kBarQEmpty + t));
+                }
+                commit_pair(bar(kBarKEmpty + kc % kKStages));
+                for (int j = 0; j < n; ++j) {
+                    const int g = kc + j;
+                    const bool nxt = j + 1 < n;
+                    const bool last_qk = j + 2 == n;
+                    const int ks = (g + 1) % kKStages, vs = g % kVStages;
+                    pair_wait(bar(kBarVReady + vs), (g / kVStages) & 1, p.wait, abort);
+                    pair_wait(bar(kBarPReady + 0), g & 1, p.wait, abort);
+                    tc_fence_after();
+                    issue_pv(0, vs, j > 0);
+                    if (nxt) {
+                        pair_wait(bar(kBarKReady + ks), ((g + 1) / kKStages) & 1, p.wait, abort);
+                        tc_fence_after();
+                        issue_qk(0, ks);
+                        commit_pair(bar(kBarSFull + 0));
+                        if (last_qk) commit_pair(bar(kBarQEmpty + 0));
+                    } else {
+                        commit_pair(bar(kBarODone + 0));
+                    }
+                    pair_wait(bar(kBarPReady + 1), g & 1, p.wait, abort);
+                    tc_fence_after();
+                    issue_pv(1, vs, j > 0);
+                    commit_pair(bar(kBarVEmpty + vs));
+                    if (nxt) {
+                        issue_qk(1, ks);
+                        commit_pair(bar(kBarSFull + 1));
+                        if (last_qk) commit_pair(bar(kBarQEmpty + 1));
+                        commit_pair(bar(kBarKEmpty + ks));
+                    } else {
+                        commit_pair(bar(kBarODone + 1));
+                    }
+                }
+                kc += n;
+            }
+        }
+    } else if (warp == kWarpRelay) {
+        // ------------------------------------------------------------ "V landed" relay (both CTAs)
+        if (lane == 0) {
+            int kc = 0;
+            for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
+                const Item it = make_item(p, w);
+                for (int j = 0; j < it.n_kt; ++j, ++kc) {
+                    pair_wait(bar(kBarVFull + kc % kVStages), (kc / kVStages) & 1, p.wait, abort);
+                    arrive_leader(bar(kBarVReady + kc % kVStages));
+                }
+            }
+        }
+    } else if (warp >= kWarpRope && warp < kWarpTma) {
+        // ------------------------------------------------------------ K RoPE (both CTAs, 64 keys each)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRope));
+        const int rt = threadIdx.x - kWarpRope * 32;
+        const int c = rt & 7, r0 = rt >> 3;
+        const int max_row = p.rope.max_pos - 1;
+        const int half0 = 64 * (int)rank;
+        KHalfRope kr;
+        kr.init(p.rope.cs, c);
+        int kc = 0;
+        for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
+            const Item it = make_item(p, w);
+            kr.load_seed(p.rope.cs, min(128 * it.j_lo + half0 + r0, max_row), c);
+            for (int j = 0; j < it.n_kt; ++j, ++kc) {
+                const int ks = kc % kKStages;
+                pair_wait(bar(kBarKFull + ks), (kc / kKStages) & 1, p.wait, abort);
+                if (!p.keys_prerotated) kr.rotate(smem + kKOff + ks * kKTile, rt);
+                if (j + 1 < it.n_kt) kr.load_seed(p.rope.cs, min(128 * (it.j_lo + j + 1) + half0 + r0, max_row), c);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) arrive_leader(bar(kBarKReady + ks));
+            }
+        }
+    } else if (warp < kWarpRope) {
+        // ------------------------------------------------------------ softmax + epilogue (both CTAs)
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+        const int t = warp >> 2;
+        const int T = 2 * (int)rank + t;       // tile of the item
+        const int i = (warp & 3) * 32 + lane;  // row of the M tile == TMEM lane
+        const int W = p.window;
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t s_addr = lane_base + col_s(t);
+        const uint32_t o_addr = lane_base + col_o(t);
+        auto rotate_q = [&](const Item &it, int k) {
+            pair_wait(bar(kBarQFull + t), k & 1, p.wait, abort);
+            rope_q_tile(smem + kQOff + t * kQTile, i, p.rope.cs, p.q_pos0 + it.r0 + T * P, p.G, P,
+                        min(P, p.S_q - (it.r0 + T * P)));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) arrive_leader(bar(kBarQReady + t));
+        };
+        int kc = 0;
+        if (item_index(0) < p.n_work) rotate_q(make_item(p, item_index(0)), 0);
+        for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
+            const Item it = make_item(p, w);
+            const int r = it.r0 + T * P + i % P;  // query row index
+            const int m = p.q_pos0 + r;           // its position
+            const bool in_prefix = m < p.prefix_len;
+            const int key_lo = (in_prefix || W <= 0) ? 0 : m - W + 1;
+            const int key_hi = in_prefix ? p.prefix_len - 1 : m;
+            float m_run = -INFINITY, l_run = 0.f;
+
+            for (int j = 0; j < it.n_kt; ++j) {
+                pair_wait(bar(kBarSFull + t), (kc + j) & 1, p.wait, abort);
+                tc_fence_after();
+                const int kstart = 128 * (it.j_lo + j);
+                const int hi_c = key_hi - kstart;
+                const int lo_c = key_lo - kstart;
+                const bool full_vis = lo_c <= 0 && hi_c >= 127;
+                const bool all_full = __all_sync(0xffffffffu, full_vis);
+                uint32_t v[128];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * ch]));
+                tmem_wait_ld();
+                if (!all_full) {
+#pragma unroll
+                    for (int e = 0; e < 128; ++e)
+                        if (e < lo_c || e > hi_c) v[e] = __float_as_uint(-INFINITY);
+                }
+                float acc[8];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) acc[a] = __uint_as_float(v[a]);
+#pragma unroll
+                for (int e = 8; e + 16 <= 128; e += 16)
+#pragma unroll
+                    for (int a = 0; a < 8; ++a)
+                        acc[a] = fmax3(acc[a], __uint_as_float(v[e + a]), __uint_as_float(v[e + 8 + a]));
+#pragma unroll
+                for (int a = 0; a < 8; ++a) acc[a] = fmaxf(acc[a], __uint_as_float(v[120 + a]));
+                const float mx =
+                    fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
+                const float m_tile = mx * p.scale_log2;
+                const float m_new = fmaxf(m_run, m_tile);
+                const bool need = (m_run != -INFINITY) && (m_new > m_run + 8.f);
+                if (__any_sync(0xffffffffu, need)) {
+                    const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
+                    l_run *= alpha;
+                    m_run = m_new;
+#pragma unroll 1
+                    for (int ch = 0; ch < D / 16; ++ch) {
+                        uint32_t o[16];
+                        tmem_ld16(o_addr + 16 * ch, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st16(o_addr + 16 * ch, o);
+                    }
+                } else if (m_run == -INFINITY) {
+                    m_run = m_new;
+                }
+                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                const uint64_t SC = f2_pack(p.scale_log2, p.scale_log2);
+                const uint64_t NM = f2_pack(-m_use, -m_use);
+                uint64_t lacc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        const uint64_t x =
+                            f2_pack(__uint_as_float(v[32 * q4 + 2 * e2]), __uint_as_float(v[32 * q4 + 2 * e2 + 1]));
+                        float y0, y1;
+                        f2_unpack(f2_fma(x, SC, NM), y0, y1);
+                        const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+                        lacc[e2 & 3] = f2_add(lacc[e2 & 3], f2_pack(p0, p1));
+                        pk[e2] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(s_addr + 16 * q4, pk);
+                }
+                {
+                    float a0, a1;
+                    f2_unpack(f2_add(f2_add(lacc[0], lacc[1]), f2_add(lacc[2], lacc[3])), a0, a1);
+                    l_run += a0 + a1;
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive_leader(bar(kBarPReady + t));
+            }
+            kc += it.n_kt;
+
+            const int w_next = item_index(k + 1);
+            if (w_next < p.n_work) rotate_q(make_item(p, w_next), k + 1);
+
+            // ---- epilogue: O / l -> bf16 -> global, one row per thread
+            pair_wait(bar(kBarODone + t), k & 1, p.wait, abort);
+            tc_fence_after();
+            const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+            const int hl = i / P;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(it.zq + hl) * p.S_q + r) * D);
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t o[32];
+                tmem_ld32(o_addr + 32 * ch, o);
+                tmem_wait_ld();
+                uint32_t w2[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w2[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                if (r < p.S_q) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        dst[4 * ch + q4] = make_uint4(w2[4 * q4], w2[4 * q4 + 1], w2[4 * q4 + 2], w2[4 * q4 + 3]);
+                }
+            }
+            tc_fence_before();
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();  // every MMA of the pair has completed and every remote arrival has landed
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_pair(const PrefillLaunch &L, cudaStream_t stream)
+{
+    if (L.p.d_h != D || (L.grid & 1)) return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err != cudaSuccess) return err;
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, prefill_pair_kernel);
+    if (err != cudaSuccess) return err;
+    if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
+    prefill_pair_kernel<<<L.grid, kThreads, kSmemBytes, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
+    return cudaGetLastError();
+}
+
+}  // namespace apex

@@ -6,9 +6,10 @@ tests, the smoke check in ``__graft_entry__`` and the CPU-baseline leg of
 with the CUDA path: the arithmetic lives in ``oracle.c`` (plain C, double
 precision), written from the formulas of "APEX-1 Mathematical Reference --
 Part 1" (§4 RoPE) and "-- Part 2" (§6 scaled dot-product attention, §8 GQA,
-§10 sliding window).  This module only compiles that file and marshals arrays.
+§9.3 decoupled RoPE, §10 sliding window).  This module only compiles that file
+and marshals arrays.
 
-Every function here is pinned by ``tests/test_oracle.py`` against the pages'
+Every function here is pinned by ``tests/test_oracle*.py`` against the pages'
 worked examples, closed forms, invariants and an independent brute force.
 """
 from __future__ import annotations
@@ -64,6 +65,11 @@ def _load():
             for name in ("oracle_attn_ex_bf16", "oracle_attn_ex_f64"):
                 fn = getattr(lib, name)
                 fn.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i64, f64, i32,
+                               vp, i32, i32, ctypes.POINTER(_Opts)]
+                fn.restype = i32
+            for name in ("oracle_mla_attn_bf16", "oracle_mla_attn_f64"):
+                fn = getattr(lib, name)
+                fn.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i64, f64, i32,
                                vp, i32, i32, ctypes.POINTER(_Opts)]
                 fn.restype = i32
             lib.oracle_yarn_theta_f64.argtypes = [i32, f64, f64, f64, f64, vp]
@@ -184,4 +190,47 @@ def attn(q, k, v, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.
             int(threads or default_threads()), ctypes.byref(opts))
     if rc != 0:
         raise ValueError("oracle_attn failed with code %d" % rc)
+    return out
+
+
+def mla_attn(q, k, v, d_rope: int, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.0,
+             causal: bool = True, rows=None, threads: int | None = None, yarn_s: float = 1.0,
+             yarn_beta_fast: float = 32.0, yarn_beta_slow: float = 1.0, prefix_len: int = 0,
+             keys_prerotated: bool = False) -> np.ndarray:
+    """Multi-head latent attention with decoupled RoPE in fp64 (Part 2, §9.3).
+
+    q [B, H_q, S_q, d_h + d_rope], k [B, H_kv, S_k, d_h + d_rope] hold
+    [content | rope part] rows; v [B, H_kv, S_k, d_h].  Only the rope part is
+    rotated (a d_rope-dimensional RoPE); scores are divided by
+    sqrt(d_h + d_rope).  Returns out [B, H_q, n_rows, d_h] (float64).  The
+    other arguments are those of attn(); keys_prerotated means the rope part of
+    k is already rotated.
+    """
+    import torch
+    bf16 = isinstance(q, torch.Tensor) and q.dtype == torch.bfloat16
+    if bf16:
+        qa, ka, va = _as_bf16_bits(q), _as_bf16_bits(k), _as_bf16_bits(v)
+        fn = _load().oracle_mla_attn_bf16
+    else:
+        cv = lambda a: np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+        qa, ka, va = cv(q), cv(k), cv(v)
+        fn = _load().oracle_mla_attn_f64
+    B, H_q, S_q, d_qk = qa.shape
+    Bk, H_kv, S_k, dk = ka.shape
+    d_h = d_qk - int(d_rope)
+    if Bk != B or dk != d_qk or va.shape != (B, H_kv, S_k, d_h) or d_h <= 0:
+        raise ValueError("shape mismatch between q, k, v for d_rope=%d" % d_rope)
+    opts = _Opts(float(yarn_s), float(yarn_beta_fast), float(yarn_beta_slow), int(prefix_len),
+                 1 if keys_prerotated else 0)
+    if rows is None:
+        rows_arr, n_rows, rows_ptr = None, S_q, None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+        n_rows, rows_ptr = int(rows_arr.shape[0]), _ptr(rows_arr)
+    out = np.empty((B, H_q, n_rows, d_h), dtype=np.float64)
+    rc = fn(_ptr(qa), _ptr(ka), _ptr(va), _ptr(out), B, H_q, H_kv, S_q, S_k, d_h, int(d_rope), int(window),
+            int(q_pos0), float(rope_base), 1 if causal else 0, rows_ptr, n_rows,
+            int(threads or default_threads()), ctypes.byref(opts))
+    if rc != 0:
+        raise ValueError("oracle_mla_attn failed with code %d" % rc)
     return out

@@ -40,6 +40,13 @@
  *     sees exactly the keys j < P; queries at m >= P follow the causal/window rule.
  *   - keys given already rotated (a KV cache holding RoPE(k, j)): the keys are
  *     used as they are.
+ *   - decoupled RoPE of multi-head latent attention (Part 2, §9.3): query and
+ *     key rows are [content (d_h) | rope part (d_r)] with length d_h + d_r,
+ *     value and output rows have length d_h; only the trailing d_r entries are
+ *     rotated, as a d_r-dimensional RoPE vector (theta_i = base^(-2i/d_r)),
+ *     and the scores are divided by sqrt(d_h + d_r), the length of the vectors
+ *     being dotted.  The plain block is the case d_r = d_h + d_r = row length,
+ *     i.e. no content part and value rows as long as query rows.
  *
  * Inputs are either raw bf16 bit patterns (widened exactly to double) or
  * doubles.  A rope_base <= 0 switches RoPE off (again only for the §6.4
@@ -155,20 +162,24 @@ static int rope_cache_build(rope_cache *c, long n_pos, int d, double base, const
  * Part 1, §4.2 / §4.4: rotate each pair (x_2i, x_2i+1) by angle m*theta_i:
  *   x'_2i   = x_2i * cos - x_2i+1 * sin
  *   x'_2i+1 = x_2i * sin + x_2i+1 * cos
- * With no cache (RoPE switched off) the vector is copied unchanged.
+ * over the trailing d_rope entries of the length-d vector (the whole vector in
+ * the plain block; the rope part of Part 2, §9.3 otherwise), whose pairs are
+ * numbered from the start of that part.  The leading d - d_rope entries are
+ * copied.  With no cache (RoPE switched off) the vector is copied unchanged.
  */
-static void rope_apply(const rope_cache *c, long m, const double *x, double *out, int d)
+static void rope_apply(const rope_cache *c, long m, const double *x, double *out, int d, int d_rope)
 {
-    if (!c->cs) {
-        memcpy(out, x, sizeof(double) * (size_t)d);
+    memcpy(out, x, sizeof(double) * (size_t)d);
+    if (!c->cs)
         return;
-    }
-    for (int i = 0; i < d / 2; ++i) {
+    const double *xr = x + (d - d_rope);
+    double *outr = out + (d - d_rope);
+    for (int i = 0; i < d_rope / 2; ++i) {
         double cs = c->cs[((size_t)m * c->half + i) * 2 + 0];
         double sn = c->cs[((size_t)m * c->half + i) * 2 + 1];
-        double x0 = x[2 * i], x1 = x[2 * i + 1];
-        out[2 * i] = x0 * cs - x1 * sn;
-        out[2 * i + 1] = x0 * sn + x1 * cs;
+        double x0 = xr[2 * i], x1 = xr[2 * i + 1];
+        outr[2 * i] = x0 * cs - x1 * sn;
+        outr[2 * i + 1] = x0 * sn + x1 * cs;
     }
 }
 
@@ -192,8 +203,11 @@ typedef struct {
     const void *q, *k, *v;
     int kind;
     double *out;
-    int B, H_q, H_kv, S_q, S_k, d, window, causal, prefix_len, keys_prerotated;
-    double score_factor; /* 1 / sqrt(d_h), times the YaRN temperature */
+    int B, H_q, H_kv, S_q, S_k, window, causal, prefix_len, keys_prerotated;
+    int d;      /* query / key row length */
+    int d_v;    /* value / output row length */
+    int d_rope; /* trailing query / key entries that RoPE rotates */
+    double score_factor; /* 1 / sqrt(d), times the YaRN temperature */
     long q_pos0;
     const int *rows;
     int n_rows;
@@ -224,7 +238,7 @@ static int row_index(const attn_job *job, int i)
 static void run_task(attn_job *job, long task, double *kbuf, double *qraw, double *qrot,
                      double *kraw, double *scores, double *acc)
 {
-    const int d = job->d;
+    const int d = job->d, d_v = job->d_v, d_rope = job->d_rope;
     const int G = job->H_q / job->H_kv;
     const int chunk_id = (int)(task % job->n_chunks);
     const int g = (int)((task / job->n_chunks) % job->H_kv);
@@ -263,7 +277,7 @@ static void run_task(attn_job *job, long task, double *kbuf, double *qraw, doubl
         if (job->keys_prerotated)
             memcpy(kbuf + (size_t)(j - j_lo) * d, kraw, sizeof(double) * (size_t)d);
         else
-            rope_apply(job->cache, j, kraw, kbuf + (size_t)(j - j_lo) * d, d);
+            rope_apply(job->cache, j, kraw, kbuf + (size_t)(j - j_lo) * d, d, d_rope);
     }
 
     for (int hh = 0; hh < G; ++hh) {
@@ -274,7 +288,7 @@ static void run_task(attn_job *job, long task, double *kbuf, double *qraw, doubl
             size_t qbase = (((size_t)b * job->H_q + h) * job->S_q + (size_t)r) * d;
             for (int e = 0; e < d; ++e)
                 qraw[e] = load_elem(job->q, qbase + e, job->kind);
-            rope_apply(job->cache, m, qraw, qrot, d);
+            rope_apply(job->cache, m, qraw, qrot, d, d_rope);
 
             /* step 4: scaled scores of the visible keys (times the YaRN temperature) */
             double M = -INFINITY;
@@ -291,9 +305,9 @@ static void run_task(attn_job *job, long task, double *kbuf, double *qraw, doubl
                 if (!any || s > M) M = s;
                 any = 1;
             }
-            double *o = job->out + (((size_t)b * job->H_q + h) * job->n_rows + (size_t)i) * d;
+            double *o = job->out + (((size_t)b * job->H_q + h) * job->n_rows + (size_t)i) * d_v;
             if (!any) { /* no visible key: left as NaN, the API forbids it */
-                for (int e = 0; e < d; ++e) o[e] = NAN;
+                for (int e = 0; e < d_v; ++e) o[e] = NAN;
                 continue;
             }
             /* step 5: Z = sum exp(s - M), then o = sum exp(s - M)/Z * v */
@@ -301,16 +315,16 @@ static void run_task(attn_job *job, long task, double *kbuf, double *qraw, doubl
             for (long j = j_lo; j <= j_hi; ++j)
                 if (key_visible(m, j, job->window, job->causal, job->prefix_len))
                     Z += exp(scores[j - j_lo] - M);
-            for (int e = 0; e < d; ++e) acc[e] = 0.0;
+            for (int e = 0; e < d_v; ++e) acc[e] = 0.0;
             for (long j = j_lo; j <= j_hi; ++j) {
                 if (!key_visible(m, j, job->window, job->causal, job->prefix_len))
                     continue;
                 double p = exp(scores[j - j_lo] - M) / Z;
-                size_t vbase = (kv_head * job->S_k + (size_t)j) * d;
-                for (int e = 0; e < d; ++e)
+                size_t vbase = (kv_head * job->S_k + (size_t)j) * d_v;
+                for (int e = 0; e < d_v; ++e)
                     acc[e] += p * load_elem(job->v, vbase + e, job->kind);
             }
-            for (int e = 0; e < d; ++e) o[e] = acc[e];
+            for (int e = 0; e < d_v; ++e) o[e] = acc[e];
         }
     }
 }
@@ -320,7 +334,7 @@ static void *worker(void *arg)
     attn_job *job = (attn_job *)arg;
     const int d = job->d;
     double *kbuf = (double *)malloc(sizeof(double) * (size_t)job->S_k * d);
-    double *scratch = (double *)malloc(sizeof(double) * (size_t)(4 * d + job->S_k));
+    double *scratch = (double *)malloc(sizeof(double) * (size_t)(3 * d + job->d_v + job->S_k));
     if (!kbuf || !scratch) {
         pthread_mutex_lock(&job->lock);
         job->status = ORACLE_ERR_NOMEM;
@@ -330,7 +344,7 @@ static void *worker(void *arg)
         return NULL;
     }
     double *qraw = scratch, *qrot = scratch + d, *kraw = scratch + 2 * d, *acc = scratch + 3 * d;
-    double *scores = scratch + 4 * d;
+    double *scores = scratch + 3 * d + job->d_v;
     for (;;) {
         long t = take_task(job);
         if (t >= job->n_tasks)
@@ -343,15 +357,16 @@ static void *worker(void *arg)
 }
 
 static int attn_common(const void *q, const void *k, const void *v, int kind, double *out,
-                       int B, int H_q, int H_kv, int S_q, int S_k, int d, int window,
-                       long q_pos0, double rope_base, int causal, const int *rows, int n_rows,
-                       int n_threads, const oracle_opts *opts)
+                       int B, int H_q, int H_kv, int S_q, int S_k, int d, int d_v, int d_rope,
+                       int window, long q_pos0, double rope_base, int causal, const int *rows,
+                       int n_rows, int n_threads, const oracle_opts *opts)
 {
     if (opts && (opts->prefix_len < 0 || opts->prefix_len > S_k ||
                  (opts->yarn_s > 1.0 && (opts->beta_fast <= 0.0 || opts->beta_slow <= 0.0))))
         return ORACLE_ERR_ARG;
     if (!q || !k || !v || !out || B <= 0 || H_q <= 0 || H_kv <= 0 || S_q <= 0 || S_k <= 0 ||
-        d <= 0 || (d & 1) || H_q % H_kv != 0 || q_pos0 < 0)
+        d <= 0 || d_v <= 0 || d_rope <= 0 || (d_rope & 1) || d_rope > d || H_q % H_kv != 0 ||
+        q_pos0 < 0)
         return ORACLE_ERR_ARG;
     if (!rows)
         n_rows = S_q;
@@ -367,13 +382,14 @@ static int attn_common(const void *q, const void *k, const void *v, int kind, do
     }
 
     rope_cache cache;
-    if (rope_cache_build(&cache, max_pos, d, rope_base, opts) != ORACLE_OK)
+    if (rope_cache_build(&cache, max_pos, d_rope, rope_base, opts) != ORACLE_OK)
         return ORACLE_ERR_NOMEM;
 
     attn_job job;
     memset(&job, 0, sizeof job);
     job.q = q; job.k = k; job.v = v; job.kind = kind; job.out = out;
     job.B = B; job.H_q = H_q; job.H_kv = H_kv; job.S_q = S_q; job.S_k = S_k; job.d = d;
+    job.d_v = d_v; job.d_rope = d_rope;
     job.window = window; job.causal = causal; job.q_pos0 = q_pos0;
     job.prefix_len = opts ? opts->prefix_len : 0;
     job.keys_prerotated = opts ? opts->keys_prerotated : 0;
@@ -458,7 +474,7 @@ int oracle_attn_ex_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                         long q_pos0, double rope_base, int causal, const int *rows, int n_rows,
                         int n_threads, const oracle_opts *opts)
 {
-    return attn_common(q, k, v, ELEM_BF16, out, B, H_q, H_kv, S_q, S_k, d, window, q_pos0,
+    return attn_common(q, k, v, ELEM_BF16, out, B, H_q, H_kv, S_q, S_k, d, d, d, window, q_pos0,
                        rope_base, causal, rows, n_rows, n_threads, opts);
 }
 
@@ -467,7 +483,7 @@ int oracle_attn_ex_f64(const double *q, const double *k, const double *v, double
                        double rope_base, int causal, const int *rows, int n_rows, int n_threads,
                        const oracle_opts *opts)
 {
-    return attn_common(q, k, v, ELEM_F64, out, B, H_q, H_kv, S_q, S_k, d, window, q_pos0,
+    return attn_common(q, k, v, ELEM_F64, out, B, H_q, H_kv, S_q, S_k, d, d, d, window, q_pos0,
                        rope_base, causal, rows, n_rows, n_threads, opts);
 }
 
@@ -476,7 +492,7 @@ int oracle_attn_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v, do
                      long q_pos0, double rope_base, int causal, const int *rows, int n_rows,
                      int n_threads)
 {
-    return attn_common(q, k, v, ELEM_BF16, out, B, H_q, H_kv, S_q, S_k, d, window, q_pos0,
+    return attn_common(q, k, v, ELEM_BF16, out, B, H_q, H_kv, S_q, S_k, d, d, d, window, q_pos0,
                        rope_base, causal, rows, n_rows, n_threads, NULL);
 }
 
@@ -485,8 +501,37 @@ int oracle_attn_f64(const double *q, const double *k, const double *v, double *o
                     int H_q, int H_kv, int S_q, int S_k, int d, int window, long q_pos0,
                     double rope_base, int causal, const int *rows, int n_rows, int n_threads)
 {
-    return attn_common(q, k, v, ELEM_F64, out, B, H_q, H_kv, S_q, S_k, d, window, q_pos0,
+    return attn_common(q, k, v, ELEM_F64, out, B, H_q, H_kv, S_q, S_k, d, d, d, window, q_pos0,
                        rope_base, causal, rows, n_rows, n_threads, NULL);
+}
+
+/*
+ * Multi-head latent attention with decoupled RoPE (Part 2, §9.3):
+ *   q   [B, H_q,  S_q, d_h + d_r]   k [B, H_kv, S_k, d_h + d_r]
+ *   v   [B, H_kv, S_k, d_h]         out [B, H_q, n_rows, d_h]
+ * Rows of q and k are [content | rope part]; RoPE (of dimension d_r) turns
+ * only the rope part, scores are divided by sqrt(d_h + d_r).
+ */
+int oracle_mla_attn_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *out,
+                         int B, int H_q, int H_kv, int S_q, int S_k, int d_h, int d_r, int window,
+                         long q_pos0, double rope_base, int causal, const int *rows, int n_rows,
+                         int n_threads, const oracle_opts *opts)
+{
+    if (d_h <= 0 || d_r <= 0)
+        return ORACLE_ERR_ARG;
+    return attn_common(q, k, v, ELEM_BF16, out, B, H_q, H_kv, S_q, S_k, d_h + d_r, d_h, d_r,
+                       window, q_pos0, rope_base, causal, rows, n_rows, n_threads, opts);
+}
+
+int oracle_mla_attn_f64(const double *q, const double *k, const double *v, double *out, int B,
+                        int H_q, int H_kv, int S_q, int S_k, int d_h, int d_r, int window,
+                        long q_pos0, double rope_base, int causal, const int *rows, int n_rows,
+                        int n_threads, const oracle_opts *opts)
+{
+    if (d_h <= 0 || d_r <= 0)
+        return ORACLE_ERR_ARG;
+    return attn_common(q, k, v, ELEM_F64, out, B, H_q, H_kv, S_q, S_k, d_h + d_r, d_h, d_r,
+                       window, q_pos0, rope_base, causal, rows, n_rows, n_threads, opts);
 }
 
 /* YaRN-scaled frequencies theta'_i, i < d/2 (Part 1, §5.3-§5.4), and the

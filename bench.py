@@ -61,8 +61,14 @@ def visible_pairs(S_q, S_k, window, q_pos0, prefix_len=0):
     return total
 
 
+def flops_per_pair(w):
+    """Tensor FLOPs of one visible (query, key) pair: 2 (d_h + d_r) for the score,
+    2 d_h for its share of P V (d_r = 0 for the plain block)."""
+    return 2.0 * (w.d_h + w.d_r) + 2.0 * w.d_h
+
+
 def prefill_flops(w, prefix_len=0):
-    return 4.0 * w.d_h * visible_pairs(w.S_q, w.S_k, w.window, w.q_pos0, prefix_len) * w.B * w.H_q
+    return flops_per_pair(w) * visible_pairs(w.S_q, w.S_k, w.window, w.q_pos0, prefix_len) * w.B * w.H_q
 
 
 def decode_kv_bytes(w, prefix_len=0):
@@ -196,14 +202,17 @@ def oracle_sample_prefill(w, q, k, v, budget_rows, batches=1):
     step = max(1, w.S_q // budget_rows)
     rows = list(range(0, w.S_q, step))
     t0 = time.perf_counter()
-    oracle.attn(q[:batches], k[:batches], v[:batches], window=w.window, q_pos0=w.q_pos0, rows=rows)
+    if w.d_r:
+        oracle.mla_attn(q[:batches], k[:batches], v[:batches], w.d_r, window=w.window, q_pos0=w.q_pos0, rows=rows)
+    else:
+        oracle.attn(q[:batches], k[:batches], v[:batches], window=w.window, q_pos0=w.q_pos0, rows=rows)
     dt = time.perf_counter() - t0
     pairs = 0
     for r in rows:
         m = w.q_pos0 + r
         lo = max(0, m - w.window + 1) if w.window > 0 else 0
         pairs += m - lo + 1
-    flops = 4.0 * w.d_h * pairs * w.H_q * batches
+    flops = flops_per_pair(w) * pairs * w.H_q * batches
     return flops, dt, "prefill %s: %d of %d sequences, all %d heads, %d of %d rows (every %d-th)" % (
         w.name, batches, w.B, w.H_q, len(rows), w.S_q, step)
 
@@ -301,9 +310,9 @@ def run_ours(args):
     if do_pre:
         pin = inp.workload_inputs(wp, pin=True)
         pq, pk, pv = (t.to(dev, non_blocking=True) for t in pin)
-        pout = torch.empty_like(pq)
+        pout = torch.empty((wp.B, wp.H_q, wp.S_q, wp.d_h), dtype=torch.bfloat16, device=dev)
         pout_h = torch.empty(pout.shape, dtype=pout.dtype, pin_memory=True)
-        apex.apex_attn_rope_reserve(wp.S_k, wp.d_h, wp.rope_base)
+        apex.apex_attn_rope_reserve(wp.S_k, wp.d_r or wp.d_h, wp.rope_base)
     if do_dec:
         din = inp.workload_inputs(dataclasses.replace(wd, S_q=1), pin=True)
         dq, dk, dv = (t.to(dev, non_blocking=True) for t in din)
@@ -315,6 +324,8 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     feat = FEATURES[args.feature]
+    if wp.d_r and feat.get("keys_prerotated"):
+        raise SystemExit("--feature prerotated rotates whole key rows; not defined for the decoupled-RoPE workload")
     if feat.get("keys_prerotated"):
         # the caches hold RoPE(k_j, j): rotate the keys once, outside the timing
         if do_pre:
@@ -324,7 +335,11 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     def prefill():
-        apex.fwd(pq, pk, pv, window=wp.window, q_pos0=wp.q_pos0, rope_base=wp.rope_base, out=pout, **feat)
+        if wp.d_r:
+            apex.mla_fwd(pq, pk, pv, wp.d_r, window=wp.window, q_pos0=wp.q_pos0, rope_base=wp.rope_base, out=pout,
+                         **feat)
+        else:
+            apex.fwd(pq, pk, pv, window=wp.window, q_pos0=wp.q_pos0, rope_base=wp.rope_base, out=pout, **feat)
 
     def decode():
         apex.decode(dq, dk, dv, wd.q_pos0, window=wd.window, rope_base=wd.rope_base, out=dout, workspace=ws,
@@ -413,8 +428,9 @@ def run_ours(args):
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
         desc = []
         if do_pre:
-            desc.append("prefill %s (B%d Hq%d Hkv%d S%d d%d W%d)" % (wp.name, wp.B, wp.H_q, wp.H_kv, wp.S_q,
-                                                                     wp.d_h, wp.window))
+            desc.append("prefill %s (B%d Hq%d Hkv%d S%d d%d%s W%d)" % (
+                wp.name, wp.B, wp.H_q, wp.H_kv, wp.S_q, wp.d_h, ("+%d decoupled RoPE" % wp.d_r) if wp.d_r else "",
+                wp.window))
         if do_dec:
             desc.append("decode (B%d Hq%d Hkv%d Sk%d d%d q_pos %d)" % (wd.B, wd.H_q, wd.H_kv, wd.S_k, wd.d_h,
                                                                         wd.q_pos0))
@@ -434,7 +450,9 @@ def run_ours(args):
             line["prefill"] = {"value": line["value"], "unit": "TFLOP/s", "ms_per_call": pre_launch_s * 1e3,
                                "frac_of_bf16": pre_achieved / peaks["bf16_tflops"],
                                "frac_of_bf16_sustained": pre_achieved / peaks["bf16_tflops_sustained"]}
-            line["roofline_prefill"] = {"kernel": "prefill_kernel", "bound": "tensor", "achieved": pre_achieved,
+            kname = "prefill_pair_kernel" if (wp.d_r or os.environ.get("APEX_ATTN_PREFILL") == "pair") \
+                else "prefill_kernel"
+            line["roofline_prefill"] = {"kernel": kname, "bound": "tensor", "achieved": pre_achieved,
                                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                         "frac": pre_achieved / peaks["bf16_tflops"],
                                         "traffic": traffic.get("prefill_" + wp.name),
@@ -506,7 +524,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--part", choices=["all", "prefill", "decode"], default="all",
                     help="run only one of the two calls per step (profiling)")
-    ap.add_argument("--prefill-workload", choices=["tiny", "gqa", "wide", "long"], default=PREFILL)
+    ap.add_argument("--prefill-workload", choices=["tiny", "gqa", "wide", "long", "mla"], default=PREFILL)
     ap.add_argument("--feature", choices=sorted(FEATURES), default="none",
                     help="run the step with one of the block's options")
     ap.add_argument("--decode-batch", type=int, default=None,

@@ -118,6 +118,30 @@ apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *
                              const apex_attn_options *opt, apex_stream_t stream);
 
 /*
+ * Prefill of multi-head latent attention with decoupled RoPE (Part 2 §9.3):
+ * query and key rows are [content | rope part], the rope part alone is
+ * rotated, and values keep the content length.
+ *
+ *   q   [B, H_q,  S_q, d_h + d_r] bf16, read     (row: q_content | q_rope)
+ *   k   [B, H_kv, S_k, d_h + d_r] bf16, read     (row: k_content | k_rope)
+ *   v   [B, H_kv, S_k, d_h]       bf16, read
+ *   out [B, H_q,  S_q, d_h]       bf16, written  (must not overlap q, k or v)
+ *
+ * The rope part is rotated as a d_r-dimensional RoPE vector (pairs numbered
+ * from its start, theta_i = b^(-2i/d_r), with the options' YaRN rule); the
+ * content part is used as it is.  Scores are the dot products of the whole
+ * rows divided by sqrt(d_h + d_r) (times the YaRN temperature).  With
+ * opt->keys_prerotated the rope part of k is taken as already rotated.  All
+ * other options and the masks are those of apex_attn_fwd_ex.
+ * Supported: d_h = 128, d_r = 64 (else APEX_ERR_UNSUPPORTED); d_r must be
+ * even and > 0 (else APEX_ERR_INVALID_ARG); H_q / H_kv as for apex_attn_fwd.
+ * Runs on pairs of CTAs (a thread-block cluster of 2).
+ */
+apex_status apex_attn_mla_fwd(const void *q, const void *k, const void *v, void *out,
+                              int B, int H_q, int H_kv, int S_q, int S_k, int d_h, int d_r,
+                              const apex_attn_options *opt, apex_stream_t stream);
+
+/*
  * Decode with options: as apex_attn_decode, with window, q_pos and rope_base
  * taken from *opt.  With a prefix and q_pos < P the query sees keys [0, P).
  * The workspace size is apex_attn_decode_workspace_bytes(...) as for

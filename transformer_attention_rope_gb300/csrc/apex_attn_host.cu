@@ -397,15 +397,12 @@ apex_status apex_attn_decode(const void *q, const void *k_cache, const void *v_c
                                stream);
 }
 
-apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
-                             int S_q, int S_k, int d_h, const apex_attn_options *opt, apex_stream_t stream)
+// Prefill of the plain block (d_qk = d_v = d_rope = d_h) or of decoupled-RoPE
+// attention (d_qk = d_v + d_rope): validation done by the callers.
+apex_status prefill_launch(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv, int S_q,
+                           int S_k, int d_qk, int d_v, int d_rope, const apex_attn_options *opt, const RopeFreq &f,
+                           apex_stream_t stream)
 {
-    if (!q || !k || !v || !out || !opt) return APEX_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return APEX_ERR_INVALID_ARG;
-    RopeFreq f;
-    if (!freq_of(*opt, &f)) return APEX_ERR_INVALID_ARG;
-    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, f.base);
-    if (s != APEX_OK) return s;
     const int q_pos0 = opt->q_pos, window = opt->window, P = opt->prefix_len;
     if (S_q <= 0 || q_pos0 < 0 || (long long)q_pos0 + S_q > (long long)S_k) return APEX_ERR_INVALID_ARG;
     if (P < 0 || P > S_k) return APEX_ERR_INVALID_ARG;
@@ -414,20 +411,22 @@ apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *
     DeviceState *st = current_state(&dev);
     if (!st) return APEX_ERR_CUDA;
     std::lock_guard<std::mutex> lk(st->mu);
-    s = init_device(*st, dev);
+    apex_status s = init_device(*st, dev);
     if (s != APEX_OK) return s;
     RopeTableView tv;
-    s = get_table(*st, d_h, f, S_k, &tv);
+    s = get_table(*st, d_rope, f, S_k, &tv);
     if (s != APEX_OK) return s;
 
+    const bool mla = d_qk != d_v;
+    if (mla && st->sm_count < 2) return APEX_ERR_UNSUPPORTED;
     const int G = H_q / H_kv;
     const int rows_per_head = 128 / G;
-    const bool pair = use_pair_prefill(d_h, st->sm_count);
+    const bool pair = mla || use_pair_prefill(d_qk, st->sm_count);
     PrefillLaunch L;
     memset(&L, 0, sizeof L);
-    if (!make_map(&L.tm_q, q, d_h, S_q, B * H_q, rows_per_head, G) ||
-        !make_map(&L.tm_k, k, d_h, S_k, B * H_kv, pair ? 64 : 128, 1) ||
-        !make_map(&L.tm_v, v, d_h, S_k, B * H_kv, 128, 1))
+    if (!make_map(&L.tm_q, q, d_qk, S_q, B * H_q, rows_per_head, G) ||
+        !make_map(&L.tm_k, k, d_qk, S_k, B * H_kv, pair ? 64 : 128, 1) ||
+        !make_map(&L.tm_v, v, d_v, S_k, B * H_kv, 128, 1))
         return APEX_ERR_CUDA;
     PrefillParams &p = L.p;
     p.out = static_cast<uint16_t *>(out);
@@ -439,7 +438,8 @@ apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *
     p.G = G;
     p.S_q = S_q;
     p.S_k = S_k;
-    p.d_h = d_h;
+    p.d_h = d_qk;
+    p.d_rope = d_rope;
     p.window = window > 0 ? window : 0;
     p.q_pos0 = q_pos0;
     p.prefix_len = P;
@@ -448,7 +448,7 @@ apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *
     const int block_rows = (pair ? 4 : 2) * rows_per_head;
     p.n_qblocks = (S_q + block_rows - 1) / block_rows;
     p.n_work = B * H_kv * p.n_qblocks;
-    p.scale_log2 = (float)(1.4426950408889634 * score_temperature(f) / sqrt((double)d_h));
+    p.scale_log2 = (float)(1.4426950408889634 * score_temperature(f) / sqrt((double)d_qk));
     if (pair) {
         L.grid = 2 * std::min(p.n_work, st->sm_count / 2);
         if (launch_prefill_pair(L, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return APEX_ERR_CUDA;
@@ -457,6 +457,32 @@ apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *
         if (launch_prefill(L, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return APEX_ERR_CUDA;
     }
     return APEX_OK;
+}
+
+apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
+                             int S_q, int S_k, int d_h, const apex_attn_options *opt, apex_stream_t stream)
+{
+    if (!q || !k || !v || !out || !opt) return APEX_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return APEX_ERR_INVALID_ARG;
+    RopeFreq f;
+    if (!freq_of(*opt, &f)) return APEX_ERR_INVALID_ARG;
+    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, f.base);
+    if (s != APEX_OK) return s;
+    return prefill_launch(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, d_h, d_h, opt, f, stream);
+}
+
+apex_status apex_attn_mla_fwd(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
+                              int S_q, int S_k, int d_h, int d_r, const apex_attn_options *opt, apex_stream_t stream)
+{
+    if (!q || !k || !v || !out || !opt) return APEX_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return APEX_ERR_INVALID_ARG;
+    if (d_r <= 0 || (d_r & 1)) return APEX_ERR_INVALID_ARG;
+    RopeFreq f;
+    if (!freq_of(*opt, &f)) return APEX_ERR_INVALID_ARG;
+    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, f.base);
+    if (s != APEX_OK) return s;
+    if (d_h != 128 || d_r != 64) return APEX_ERR_UNSUPPORTED;
+    return prefill_launch(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h + d_r, d_h, d_r, opt, f, stream);
 }
 
 apex_status apex_attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,

@@ -70,6 +70,7 @@ struct PrefillParams {
     int n_qblocks;       // position blocks per (b, kv-head); a block = 2 M tiles (4 on CTA pairs)
     int n_work;          // B * H_kv * n_qblocks (work items, walked by a persistent grid)
     float scale_log2;    // log2(e) / sqrt(d_h)
+    int d_rope;          // trailing entries of a q / k row that RoPE turns (d_h: all)
 };
 
 struct PrefillLaunch {
@@ -79,7 +80,9 @@ struct PrefillLaunch {
 };
 
 cudaError_t launch_prefill(const PrefillLaunch &L, cudaStream_t stream);
-// CTA-pair variant (d_h = 128): tm_k's box is {64, 64, 1}, grid even, blocks of 4 M tiles
+// CTA-pair variant: tm_k's box is {64, 64, 1}, grid even, blocks of 4 M tiles; value and
+// output rows of 128; (d_h, d_rope) = (128, 128) for the plain block or (192, 64) for
+// decoupled RoPE (d_h is then the q / k row length)
 cudaError_t launch_prefill_pair(const PrefillLaunch &L, cudaStream_t stream);
 
 // ----------------------------------------------------------------- key rotation

@@ -1,4 +1,8 @@
-// prefill_pair.cu -- the prefill on CTA pairs (tcgen05 cta_group::2), d_h = 128.
+// prefill_pair.cu -- the prefill on CTA pairs (tcgen05 cta_group::2), value and
+// output rows of 128 entries; query and key rows of DQK = 128 entries (the
+// plain block, RoPE over the whole row) or 192 (multi-head latent attention with
+// decoupled RoPE, Part 2, §9.3: rows [content (128) | rope part (64)], RoPE of
+// dimension 64 on the rope part only).
 //
 // Same computation as prefill.cu (RoPE on Q and K tiles in shared memory, GQA
 // packing of the G heads that share a KV head into each 128-row M tile, online
@@ -28,50 +32,59 @@
 namespace apex {
 namespace {
 
-constexpr int D = 128;
+constexpr int DV = 128;  // value / output row length
 constexpr int kThreads = 16 * 32;
 constexpr int kWarpRope = 8;
 constexpr int kWarpTma = 12;
 constexpr int kWarpMma = 13;
 constexpr int kWarpRelay = 14;
-constexpr int kKStages = 4;
-constexpr int kVStages = 4;
 constexpr int kLaunchRegs = 128;
 constexpr int kRegsSoftmax = 168;
 constexpr int kRegsRope = 88;
 constexpr int kRegsCtl = 88;
 static_assert(128 * (2 * kRegsSoftmax + kRegsRope + kRegsCtl) <= kThreads * kLaunchRegs, "register split");
 
-constexpr int kQBox = 128 * 128;                 // [128 rows][64 dims]
-constexpr int kQTile = 2 * kQBox;                // 128 x 128
-constexpr int kKBox = 64 * 128;                  // [64 keys][64 dims]
-constexpr int kKTile = 2 * kKBox;                // this CTA's 64 keys x 128 dims
-constexpr int kVTile = 128 * 128;                // 128 keys x this CTA's 64 dims
-// Q | V stages | K stages | 8 KB guard | barriers: an operand descriptor that
-// walked past its tile (it should not: each CTA's B half is 64 rows or 64
-// columns) would still stay inside the allocation.
-constexpr int kQOff = 0;
-constexpr int kVOff = 2 * kQTile;
-constexpr int kKOff = kVOff + kVStages * kVTile;
-constexpr int kBarOff = kKOff + kKStages * kKTile + 8192;
+constexpr int kQBox = 128 * 128;  // [128 rows][64 dims]
+constexpr int kKBox = 64 * 128;   // [64 keys][64 dims]
+constexpr int kVTile = 128 * 128; // 128 keys x this CTA's 64 dims
 
-// barrier slots
-constexpr int kBarQFull = 0;                         // [2]  local TMA
-constexpr int kBarQReady = 2;                        // [2]  leader: 8 warps (both CTAs)
-constexpr int kBarQEmpty = 4;                        // [2]  multicast commit
-constexpr int kBarSFull = 6;                         // [2]  multicast commit
-constexpr int kBarPReady = 8;                        // [2]  leader: 8 warps
-constexpr int kBarODone = 10;                        // [2]  multicast commit
-constexpr int kBarKFull = 12;                        // [K]  local TMA
-constexpr int kBarKReady = kBarKFull + kKStages;     // [K]  leader: 8 warps
-constexpr int kBarKEmpty = kBarKReady + kKStages;    // [K]  multicast commit
-constexpr int kBarVFull = kBarKEmpty + kKStages;     // [V]  local TMA
-constexpr int kBarVReady = kBarVFull + kVStages;     // [V]  leader: 2 relays
-constexpr int kBarVEmpty = kBarVReady + kVStages;    // [V]  multicast commit
-constexpr int kNumBars = kBarVEmpty + kVStages;
-constexpr int kTmemSlot = kBarOff + kNumBars * 8;
-constexpr int kSmemBytes = kTmemSlot + 16 + 1024;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+// DQK: query / key row length; DR: trailing entries of those rows that RoPE turns.
+template <int DQK, int DR>
+struct PairCfg {
+    static_assert(DQK % 64 == 0 && DR % 64 == 0 && DR <= DQK, "row split");
+    static constexpr int kBoxes = DQK / 64;          // 64-dim boxes of a Q or K row
+    static constexpr int kRopeBox0 = (DQK - DR) / 64; // first box of the rope part
+    static constexpr int kRopeBoxes = DR / 64;
+    static constexpr int kStages = DQK > 128 ? 3 : 4;
+    static constexpr int kKStages = kStages;
+    static constexpr int kVStages = kStages;
+    static constexpr int kQTile = kBoxes * kQBox;     // 128 rows x DQK
+    static constexpr int kKTile = kBoxes * kKBox;     // this CTA's 64 keys x DQK
+    // Q | V stages | K stages | 8 KB guard | barriers: an operand descriptor that
+    // walked past its tile (it should not: each CTA's B half is 64 rows or 64
+    // columns) would still stay inside the allocation.
+    static constexpr int kQOff = 0;
+    static constexpr int kVOff = 2 * kQTile;
+    static constexpr int kKOff = kVOff + kVStages * kVTile;
+    static constexpr int kBarOff = kKOff + kKStages * kKTile + 8192;
+    // barrier slots
+    static constexpr int kBarQFull = 0;                         // [2]  local TMA
+    static constexpr int kBarQReady = 2;                        // [2]  leader: 8 warps (both CTAs)
+    static constexpr int kBarQEmpty = 4;                        // [2]  multicast commit
+    static constexpr int kBarSFull = 6;                         // [2]  multicast commit
+    static constexpr int kBarPReady = 8;                        // [2]  leader: 8 warps
+    static constexpr int kBarODone = 10;                        // [2]  multicast commit
+    static constexpr int kBarKFull = 12;                        // [K]  local TMA
+    static constexpr int kBarKReady = kBarKFull + kKStages;     // [K]  leader: 8 warps
+    static constexpr int kBarKEmpty = kBarKReady + kKStages;    // [K]  multicast commit
+    static constexpr int kBarVFull = kBarKEmpty + kKStages;     // [V]  local TMA
+    static constexpr int kBarVReady = kBarVFull + kVStages;     // [V]  leader: 2 relays
+    static constexpr int kBarVEmpty = kBarVReady + kVStages;    // [V]  multicast commit
+    static constexpr int kNumBars = kBarVEmpty + kVStages;
+    static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kTmemSlot + 16 + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
 
 __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u + 128u * t; }
@@ -180,19 +193,23 @@ __device__ __forceinline__ uint4 rope_chunk(uint4 v, const uint64_t (&C)[2], con
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// This CTA's half of a K tile: 64 key rows (position pos0 + r), stored as two
-// [64 rows][64 dims] swizzled boxes.  Thread rt owns chunk c = rt & 7 of rows
-// r0 + 16 k (r0 = rt >> 3, k < 4); the angle advances by 16 positions per
-// step: z_{k+1} = z_k * (cos 16 theta, sin 16 theta), seeded per tile.
+// This CTA's half of a K tile: 64 key rows (position pos0 + r), stored as
+// 64-dim swizzled boxes of [64 rows][64 dims]; RoPE turns boxes B0 .. B0+NRB-1,
+// whose pairs are numbered from the start of the rope part (table rows hold
+// DR/2 = 32 NRB pairs).  Thread rt owns chunk c = rt & 7 of rows r0 + 16 k
+// (r0 = rt >> 3, k < 4); the angle advances by 16 positions per step:
+// z_{k+1} = z_k * (cos 16 theta, sin 16 theta), seeded per tile.
+template <int NRB, int B0>
 struct KHalfRope {
-    uint64_t WC[2][2], WS[2][2];
-    float4 seed[2][2];
+    static constexpr int kHalf = 32 * NRB;  // pairs per table row
+    uint64_t WC[NRB][2], WS[NRB][2];
+    float4 seed[NRB][2];
 
     __device__ __forceinline__ void init(const float2 *table, int c)
     {
 #pragma unroll
-        for (int bx = 0; bx < 2; ++bx) {
-            const float4 *p = reinterpret_cast<const float4 *>(table + 16 * (D / 2) + 32 * bx + 4 * c);
+        for (int bx = 0; bx < NRB; ++bx) {
+            const float4 *p = reinterpret_cast<const float4 *>(table + 16 * kHalf + 32 * bx + 4 * c);
             const float4 a = __ldg(p), b = __ldg(p + 1);
             WC[bx][0] = f2_pack(a.x, a.z);
             WS[bx][0] = f2_pack(a.y, a.w);
@@ -203,8 +220,8 @@ struct KHalfRope {
     __device__ __forceinline__ void load_seed(const float2 *table, int pos, int c)
     {
 #pragma unroll
-        for (int bx = 0; bx < 2; ++bx) {
-            const float4 *p = reinterpret_cast<const float4 *>(table + (size_t)pos * (D / 2) + 32 * bx + 4 * c);
+        for (int bx = 0; bx < NRB; ++bx) {
+            const float4 *p = reinterpret_cast<const float4 *>(table + (size_t)pos * kHalf + 32 * bx + 4 * c);
             seed[bx][0] = __ldg(p);
             seed[bx][1] = __ldg(p + 1);
         }
@@ -212,9 +229,9 @@ struct KHalfRope {
     __device__ __forceinline__ void rotate(uint8_t *tile, int rt)
     {
         const int c = rt & 7, r0 = rt >> 3;
-        uint64_t C[2][2], S[2][2];
+        uint64_t C[NRB][2], S[NRB][2];
 #pragma unroll
-        for (int bx = 0; bx < 2; ++bx) {
+        for (int bx = 0; bx < NRB; ++bx) {
             C[bx][0] = f2_pack(seed[bx][0].x, seed[bx][0].z);
             S[bx][0] = f2_pack(seed[bx][0].y, seed[bx][0].w);
             C[bx][1] = f2_pack(seed[bx][1].x, seed[bx][1].z);
@@ -224,8 +241,8 @@ struct KHalfRope {
         for (int k = 0; k < 4; ++k) {
             const int row = r0 + 16 * k;
 #pragma unroll
-            for (int bx = 0; bx < 2; ++bx) {
-                uint4 *ptr = reinterpret_cast<uint4 *>(tile + bx * kKBox + swz128(row, c));
+            for (int bx = 0; bx < NRB; ++bx) {
+                uint4 *ptr = reinterpret_cast<uint4 *>(tile + (B0 + bx) * kKBox + swz128(row, c));
                 *ptr = rope_chunk(*ptr, C[bx], S[bx]);
                 if (k < 3) {
 #pragma unroll
@@ -243,16 +260,19 @@ struct KHalfRope {
 
 // Q tile: head-major rows (row = head * P + p); all G heads of position p share
 // one set of angles.  Thread rt takes the (p, chunk) combos rt, rt + 128, ...
+// and turns boxes B0 .. B0+NRB-1 (the rope part) of that chunk.
+template <int NRB, int B0>
 __device__ __forceinline__ void rope_q_tile(uint8_t *tile, int rt, const float2 *table, int pos0, int G, int P,
                                             int valid_p)
 {
+    constexpr int kHalf = 32 * NRB;
     for (int q = rt; q < P * 8; q += 128) {
         const int pp = q >> 3, c = q & 7;
         if (pp >= valid_p) continue;
-        uint64_t C[2][2], S[2][2];
+        uint64_t C[NRB][2], S[NRB][2];
 #pragma unroll
-        for (int bx = 0; bx < 2; ++bx) {
-            const float4 *t = reinterpret_cast<const float4 *>(table + (size_t)(pos0 + pp) * (D / 2) + 32 * bx + 4 * c);
+        for (int bx = 0; bx < NRB; ++bx) {
+            const float4 *t = reinterpret_cast<const float4 *>(table + (size_t)(pos0 + pp) * kHalf + 32 * bx + 4 * c);
             const float4 a = __ldg(t), b = __ldg(t + 1);
             C[bx][0] = f2_pack(a.x, a.z);
             S[bx][0] = f2_pack(a.y, a.w);
@@ -262,8 +282,8 @@ __device__ __forceinline__ void rope_q_tile(uint8_t *tile, int rt, const float2 
         for (int hl = 0; hl < G; ++hl) {
             const int row = hl * P + pp;
 #pragma unroll
-            for (int bx = 0; bx < 2; ++bx) {
-                uint4 *ptr = reinterpret_cast<uint4 *>(tile + bx * kQBox + swz128(row, c));
+            for (int bx = 0; bx < NRB; ++bx) {
+                uint4 *ptr = reinterpret_cast<uint4 *>(tile + (B0 + bx) * kQBox + swz128(row, c));
                 *ptr = rope_chunk(*ptr, C[bx], S[bx]);
             }
         }
@@ -303,10 +323,20 @@ __device__ __forceinline__ int item_index(int k)
     return k * g + ((k & 1) ? (g - 1 - c) : c);
 }
 
+template <int DQK, int DR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const PrefillParams p)
 {
+    using C = PairCfg<DQK, DR>;
+    constexpr int kKStages = C::kKStages, kVStages = C::kVStages;
+    constexpr int kQTile = C::kQTile, kKTile = C::kKTile;
+    constexpr int kQOff = C::kQOff, kKOff = C::kKOff, kVOff = C::kVOff, kBarOff = C::kBarOff;
+    constexpr int kTmemSlot = C::kTmemSlot;
+    constexpr int kBarQFull = C::kBarQFull, kBarQReady = C::kBarQReady, kBarQEmpty = C::kBarQEmpty;
+    constexpr int kBarSFull = C::kBarSFull, kBarPReady = C::kBarPReady, kBarODone = C::kBarODone;
+    constexpr int kBarKFull = C::kBarKFull, kBarKReady = C::kBarKReady, kBarKEmpty = C::kBarKEmpty;
+    constexpr int kBarVFull = C::kBarVFull, kBarVReady = C::kBarVReady, kBarVEmpty = C::kBarVEmpty;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const uint32_t sb = smem_u32(smem);
@@ -363,7 +393,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     pair_wait(bar(kBarQEmpty + t), (k & 1) ^ 1, p.wait, abort);
                     mbar_arrive_expect_tx(bar(kBarQFull + t), kQTile);
 #pragma unroll
-                    for (int bx = 0; bx < 2; ++bx)
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
                         tma_load_3d(sb + kQOff + t * kQTile + bx * kQBox, &tm_q, bar(kBarQFull + t), 64 * bx,
                                     it.r0 + (2 * (int)rank + t) * P, it.zq);
                 }
@@ -373,7 +403,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     pair_wait(bar(kBarKEmpty + ks), ((kc / kKStages) & 1) ^ 1, p.wait, abort);
                     mbar_arrive_expect_tx(bar(kBarKFull + ks), kKTile);
 #pragma unroll
-                    for (int bx = 0; bx < 2; ++bx)
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
                         tma_load_3d(sb + kKOff + ks * kKTile + bx * kKBox, &tm_k, bar(kBarKFull + ks), 64 * bx,
                                     key0 + 64 * (int)rank, it.unit);
                     pair_wait(bar(kBarVEmpty + vs), ((kc / kVStages) & 1) ^ 1, p.wait, abort);
@@ -391,7 +421,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t qa = sb + kQOff + t * kQTile;
                 const uint32_t kb = sb + kKOff + ks * kKTile;
 #pragma unroll
-                for (int s = 0; s < D / 16; ++s)
+                for (int s = 0; s < DQK / 16; ++s)
                     mma_ss_pair(tmem + col_s(t), smem_desc_sw128(qa + (s >> 2) * kQBox + (s & 3) * 32, 16, 1024),
                                 smem_desc_sw128(kb + (s >> 2) * kKBox + (s & 3) * 32, 16, 1024), idesc_qk,
                                 s > 0 ? 1u : 0u);
@@ -469,7 +499,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int c = rt & 7, r0 = rt >> 3;
         const int max_row = p.rope.max_pos - 1;
         const int half0 = 64 * (int)rank;
-        KHalfRope kr;
+        KHalfRope<C::kRopeBoxes, C::kRopeBox0> kr;
         kr.init(p.rope.cs, c);
         int kc = 0;
         for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
@@ -497,8 +527,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t o_addr = lane_base + col_o(t);
         auto rotate_q = [&](const Item &it, int k) {
             pair_wait(bar(kBarQFull + t), k & 1, p.wait, abort);
-            rope_q_tile(smem + kQOff + t * kQTile, i, p.rope.cs, p.q_pos0 + it.r0 + T * P, p.G, P,
-                        min(P, p.S_q - (it.r0 + T * P)));
+            rope_q_tile<C::kRopeBoxes, C::kRopeBox0>(smem + kQOff + t * kQTile, i, p.rope.cs,
+                                                     p.q_pos0 + it.r0 + T * P, p.G, P,
+                                                     min(P, p.S_q - (it.r0 + T * P)));
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) arrive_leader(bar(kBarQReady + t));
@@ -552,7 +583,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     l_run *= alpha;
                     m_run = m_new;
 #pragma unroll 1
-                    for (int ch = 0; ch < D / 16; ++ch) {
+                    for (int ch = 0; ch < DV / 16; ++ch) {
                         uint32_t o[16];
                         tmem_ld16(o_addr + 16 * ch, o);
                         tmem_wait_ld();
@@ -602,9 +633,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
             const int hl = i / P;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(it.zq + hl) * p.S_q + r) * D);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(it.zq + hl) * p.S_q + r) * DV);
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
+            for (int ch = 0; ch < DV / 32; ++ch) {
                 uint32_t o[32];
                 tmem_ld32(o_addr + 32 * ch, o);
                 tmem_wait_ld();
@@ -631,19 +662,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 }
 
+template <int DQK, int DR>
+cudaError_t launch_pair_t(const PrefillLaunch &L, cudaStream_t stream)
+{
+    using C = PairCfg<DQK, DR>;
+    cudaError_t err = cudaFuncSetAttribute(prefill_pair_kernel<DQK, DR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           C::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    // setmaxnreg.inc blocks until the block's own pool can serve it: never
+    // launch unless the split fits the registers the block is launched with
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, prefill_pair_kernel<DQK, DR>);
+    if (err != cudaSuccess) return err;
+    if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
+    prefill_pair_kernel<DQK, DR><<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_pair(const PrefillLaunch &L, cudaStream_t stream)
 {
-    if (L.p.d_h != D || (L.grid & 1)) return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (err != cudaSuccess) return err;
-    cudaFuncAttributes fa;
-    err = cudaFuncGetAttributes(&fa, prefill_pair_kernel);
-    if (err != cudaSuccess) return err;
-    if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-    prefill_pair_kernel<<<L.grid, kThreads, kSmemBytes, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
-    return cudaGetLastError();
+    if (L.grid & 1) return cudaErrorInvalidValue;
+    if (L.p.d_h == 128 && L.p.d_rope == 128) return launch_pair_t<128, 128>(L, stream);
+    if (L.p.d_h == 192 && L.p.d_rope == 64) return launch_pair_t<192, 64>(L, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace apex

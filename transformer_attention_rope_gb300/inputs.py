@@ -42,6 +42,7 @@ class Workload:
     seed: int
     decode: bool = False
     rope_base: float = 10000.0
+    d_r: int = 0         # > 0: decoupled RoPE; q / k rows hold d_h + d_r entries, v rows d_h
 
     @property
     def G(self) -> int:
@@ -59,6 +60,8 @@ WORKLOADS = {
     "long": Workload("long", 1, 32, 8, 65536, 65536, 128, 4096, 0, 3),
     # single-query decode at position 32767 against a 32768-entry KV cache
     "decode": Workload("decode", 64, 32, 8, 1, 32768, 128, 0, 32767, 4, decode=True),
+    # global-layer prefill of multi-head latent attention with a 64-entry decoupled RoPE part
+    "mla": Workload("mla", 1, 128, 8, 8192, 8192, 128, 0, 0, 5, d_r=64),
 }
 
 
@@ -92,13 +95,14 @@ def normal_bf16(shape, seed: int, stream: int, *, pin: bool = False) -> torch.Te
 
 
 def make_qkv(B: int, H_q: int, H_kv: int, S_q: int, S_k: int, d_h: int, seed: int,
-             *, pin: bool = False):
-    """Q [B,H_q,S_q,d_h], K and V [B,H_kv,S_k,d_h], bf16 on the CPU (drawn Q, K, V)."""
-    q = normal_bf16((B, H_q, S_q, d_h), seed, 0, pin=pin)
-    k = normal_bf16((B, H_kv, S_k, d_h), seed, 1, pin=pin)
+             *, pin: bool = False, d_r: int = 0):
+    """Q [B,H_q,S_q,d_h+d_r], K [B,H_kv,S_k,d_h+d_r], V [B,H_kv,S_k,d_h], bf16 on the CPU
+    (drawn Q, K, V)."""
+    q = normal_bf16((B, H_q, S_q, d_h + d_r), seed, 0, pin=pin)
+    k = normal_bf16((B, H_kv, S_k, d_h + d_r), seed, 1, pin=pin)
     v = normal_bf16((B, H_kv, S_k, d_h), seed, 2, pin=pin)
     return q, k, v
 
 
 def workload_inputs(w: Workload, *, pin: bool = False):
-    return make_qkv(w.B, w.H_q, w.H_kv, w.S_q, w.S_k, w.d_h, w.seed, pin=pin)
+    return make_qkv(w.B, w.H_q, w.H_kv, w.S_q, w.S_k, w.d_h, w.seed, pin=pin, d_r=w.d_r)

@@ -153,6 +153,26 @@ apex_status apex_attn_decode_ex(const void *q, const void *k_cache, const void *
                                 size_t workspace_bytes, apex_stream_t stream);
 
 /*
+ * Decode of multi-head latent attention with decoupled RoPE (Part 2 §9.3):
+ * one query per sequence against a cache of [content | rope part] keys.
+ *
+ *   q       [B, H_q,  1,   d_h + d_r] bf16, read   (the query sits at opt->q_pos)
+ *   k_cache [B, H_kv, S_k, d_h + d_r] bf16, read   (key j at position j)
+ *   v_cache [B, H_kv, S_k, d_h]       bf16, read
+ *   out     [B, H_q,  1,   d_h]       bf16, written
+ *   workspace: at least apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_h)
+ *           bytes (d_h: the value row length), 16-byte aligned.
+ *
+ * Rotation, scores and options as for apex_attn_mla_fwd; the result equals
+ * apex_attn_mla_fwd with S_q = 1 and q_pos0 = q_pos (up to the order of fp32
+ * sums).  Supported: d_h = 128, d_r = 64.
+ */
+apex_status apex_attn_mla_decode(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                 int B, int H_q, int H_kv, int S_k, int d_h, int d_r,
+                                 const apex_attn_options *opt, void *workspace, size_t workspace_bytes,
+                                 apex_stream_t stream);
+
+/*
  * Rotate keys for a pre-rotated KV cache (Part 1 §4.2-§4.4, with the options'
  * rope_base / YaRN): for each of n_heads heads h and each s < n_pos,
  *   k_out[h * out_head_stride + s * d_h + :] = RoPE(k_in[h * in_head_stride + s * d_h + :], pos0 + s)

@@ -109,3 +109,68 @@ def test_mla_rejects_unsupported():
     q, k, v = [t.to(dev) for t in inputs.make_qkv(1, 4, 2, 64, 64, D_H, 1901, d_r=D_R)]
     with pytest.raises(apex.ApexError):
         apex.mla_fwd(q, k, v, D_R, prefix_len=65)
+
+
+DECODE_CASES = [  # B, H_q, H_kv, S_k, window, q_pos, prefix
+    (2, 8, 2, 1000, 0, 999, 0),
+    (3, 16, 4, 777, 100, 700, 0),
+    (2, 32, 2, 600, 0, 599, 0),        # G=16: two query tiles per warp
+    (2, 8, 8, 650, 64, 649, 0),        # G=1
+    (2, 8, 2, 600, 0, 150, 400),       # query inside the prefix
+    (1, 32, 8, 4096, 1024, 4095, 0),
+]
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,S_k,window,q_pos,prefix", DECODE_CASES)
+def test_mla_decode_matches_oracle(B, H_q, H_kv, S_k, window, q_pos, prefix):
+    dev = _dev()
+    q, k, v = inputs.make_qkv(B, H_q, H_kv, 1, S_k, D_H, 2000 + S_k + q_pos, d_r=D_R)
+    out = apex.mla_decode(q.to(dev), k.to(dev), v.to(dev), q_pos, D_R, window=window, prefix_len=prefix)
+    torch.cuda.synchronize()
+    assert out.shape == (B, H_q, 1, D_H)
+    ref = oracle.mla_attn(q, k, v, D_R, window=window, q_pos0=q_pos, prefix_len=prefix)
+    _close(out, ref, "mla decode")
+    assert apex.apex_attn_device_status() == 0
+
+
+def test_mla_decode_yarn_and_prerotated():
+    dev = _dev()
+    S_k = 900
+    q, k, v = inputs.make_qkv(2, 16, 4, 1, S_k, D_H, 2100, d_r=D_R)
+    out = apex.mla_decode(q.to(dev), k.to(dev), v.to(dev), S_k - 1, D_R, yarn_scale=16.0, yarn_beta_fast=8.0,
+                          yarn_beta_slow=2.0)
+    torch.cuda.synchronize()
+    _close(out, oracle.mla_attn(q, k, v, D_R, q_pos0=S_k - 1, yarn_s=16.0, yarn_beta_fast=8.0, yarn_beta_slow=2.0),
+           "mla decode yarn")
+    kd = k.double().numpy()
+    pos = np.broadcast_to(np.arange(S_k)[None, None, :], (2, 4, S_k)).reshape(-1)
+    kd[..., D_H:] = oracle.rope(kd[..., D_H:].reshape(-1, D_R), pos).reshape(2, 4, S_k, D_R)
+    k_rot = torch.from_numpy(kd).to(torch.bfloat16)
+    out2 = apex.mla_decode(q.to(dev), k_rot.to(dev), v.to(dev), S_k - 1, D_R, window=200, keys_prerotated=True)
+    torch.cuda.synchronize()
+    _close(out2, oracle.mla_attn(q, k_rot, v, D_R, q_pos0=S_k - 1, window=200, keys_prerotated=True),
+           "mla decode prerotated")
+
+
+def test_mla_decode_equals_last_prefill_row():
+    dev = _dev()
+    S = 700
+    q, k, v = [t.to(dev) for t in inputs.make_qkv(2, 16, 4, S, S, D_H, 2200, d_r=D_R)]
+    pre = apex.mla_fwd(q, k, v, D_R, window=300)
+    dec = apex.mla_decode(q[:, :, S - 1:S].contiguous(), k, v, S - 1, D_R, window=300)
+    torch.cuda.synchronize()
+    d = (pre[:, :, S - 1:S].float() - dec.float()).abs()
+    assert d.max().item() <= 2e-2 and d.mean().item() <= 2e-3
+
+
+def test_mla_decode_full_size_sampled_sequences():
+    """The decode workload's cache shape (B64 H_q32 H_kv8 S_k 32768) with
+    decoupled-RoPE rows; the oracle checks two of the 64 sequences."""
+    dev = _dev()
+    w = inputs.WORKLOADS["decode"]
+    q, k, v = inputs.make_qkv(w.B, w.H_q, w.H_kv, 1, w.S_k, D_H, 2300, d_r=D_R)
+    out = apex.mla_decode(q.to(dev), k.to(dev), v.to(dev), w.q_pos0, D_R)
+    torch.cuda.synchronize()
+    pick = [0, 37]
+    ref = oracle.mla_attn(q[pick], k[pick], v[pick], D_R, q_pos0=w.q_pos0)
+    _close(out[pick].cpu(), ref, "mla decode full")

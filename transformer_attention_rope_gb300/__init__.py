@@ -8,9 +8,11 @@ There is no CPU fallback -- if the library is missing, every call raises.
 Raw C-ABI names (pointers and sizes):
     apex_attn_fwd, apex_attn_decode, apex_attn_decode_noalloc, apex_attn_decode_workspace_bytes,
     apex_attn_rope_reserve, apex_attn_device_status, apex_attn_status_string,
-    apex_attn_fwd_ex, apex_attn_decode_ex, apex_attn_rope_keys, apex_attn_mla_fwd (with an Options struct)
+    apex_attn_fwd_ex, apex_attn_decode_ex, apex_attn_rope_keys, apex_attn_mla_fwd, apex_attn_mla_decode
+    (with an Options struct)
 Tensor conveniences (torch, bf16, contiguous, on the current CUDA device):
-    fwd(q, k, v, ...), decode(q, k_cache, v_cache, q_pos, ...), rope_keys(k, ...), mla_fwd(q, k, v, d_r, ...)
+    fwd(q, k, v, ...), decode(q, k_cache, v_cache, q_pos, ...), rope_keys(k, ...), mla_fwd(q, k, v, d_r, ...),
+    mla_decode(q, k_cache, v_cache, q_pos, d_r, ...)
 """
 from __future__ import annotations
 
@@ -22,7 +24,8 @@ __all__ = [
     "ApexError", "library_path", "load_library", "apex_attn_fwd", "apex_attn_decode", "apex_attn_decode_noalloc",
     "apex_attn_decode_workspace_bytes", "apex_attn_rope_reserve", "apex_attn_device_status",
     "apex_attn_status_string", "apex_attn_fwd_ex", "apex_attn_decode_ex", "apex_attn_rope_keys",
-    "apex_attn_mla_fwd", "Options", "fwd", "decode", "decode_workspace_bytes", "rope_keys", "mla_fwd",
+    "apex_attn_mla_fwd", "apex_attn_mla_decode", "Options", "fwd", "decode", "decode_workspace_bytes",
+    "rope_keys", "mla_fwd", "mla_decode",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +77,8 @@ def load_library():
             lib.apex_attn_fwd_ex.restype = i32
             lib.apex_attn_mla_fwd.argtypes = [vp, vp, vp, vp] + [i32] * 7 + [op, vp]
             lib.apex_attn_mla_fwd.restype = i32
+            lib.apex_attn_mla_decode.argtypes = [vp, vp, vp, vp] + [i32] * 6 + [op, vp, sz, vp]
+            lib.apex_attn_mla_decode.restype = i32
             lib.apex_attn_decode_ex.argtypes = [vp, vp, vp, vp] + [i32] * 5 + [op, vp, sz, vp]
             lib.apex_attn_decode_ex.restype = i32
             lib.apex_attn_rope_keys.argtypes = [vp, vp] + [i32] * 4 + [ctypes.c_longlong] * 2 + [op, vp]
@@ -116,6 +121,13 @@ def apex_attn_fwd_ex(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, opt, stream) -> 
 def apex_attn_mla_fwd(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, d_r, opt, stream) -> int:
     return load_library().apex_attn_mla_fwd(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, d_r,
                                             ctypes.byref(opt) if opt is not None else None, stream)
+
+
+def apex_attn_mla_decode(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, d_r, opt, workspace,
+                         workspace_bytes, stream) -> int:
+    return load_library().apex_attn_mla_decode(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, d_r,
+                                               ctypes.byref(opt) if opt is not None else None, workspace,
+                                               workspace_bytes, stream)
 
 
 def apex_attn_decode_ex(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, opt, workspace, workspace_bytes,
@@ -253,6 +265,36 @@ def decode(q, k_cache, v_cache, q_pos: int, *, window: int = 0, rope_base: float
                                  H_kv, S_k, d, opt, workspace.data_ptr(), ws_bytes, _stream_handle(stream))
     if st != APEX_OK:
         raise ApexError(st, "apex_attn_decode")
+    return out
+
+
+def mla_decode(q, k_cache, v_cache, q_pos: int, d_r: int, *, window: int = 0, rope_base: float = 10000.0,
+               out=None, workspace=None, stream=None, yarn_scale: float = 1.0, yarn_beta_fast: float = 32.0,
+               yarn_beta_slow: float = 1.0, prefix_len: int = 0, keys_prerotated: bool = False):
+    """Decoupled-RoPE decode. q [B,H_q,1,d_h+d_r], k_cache [B,H_kv,S_k,d_h+d_r], v_cache [B,H_kv,S_k,d_h]
+    (bf16, CUDA; rows [content | rope part]) -> out [B,H_q,1,d_h]."""
+    import torch
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, 4)
+    B, H_q, one, d_qk = q.shape
+    _, H_kv, S_k, d_h = v_cache.shape
+    if one != 1:
+        raise ValueError("decode takes one query per sequence")
+    if d_qk != d_h + d_r or k_cache.shape[-1] != d_qk:
+        raise ValueError("q / k_cache rows must hold d_h + d_r entries")
+    if out is None:
+        out = torch.empty((B, H_q, 1, d_h), dtype=torch.bfloat16, device=q.device)
+    _check(out, "out", 4)
+    need = decode_workspace_bytes(B, H_q, H_kv, S_k, d_h)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    opt = _options(window, q_pos, rope_base, yarn_scale, yarn_beta_fast, yarn_beta_slow, prefix_len,
+                   keys_prerotated)
+    st = apex_attn_mla_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), B, H_q, H_kv,
+                              S_k, d_h, int(d_r), opt, workspace.data_ptr(), ws_bytes, _stream_handle(stream))
+    if st != APEX_OK:
+        raise ApexError(st, "apex_attn_mla_decode")
     return out
 
 

@@ -311,45 +311,40 @@ size_t apex_attn_decode_workspace_bytes(int B, int H_q, int H_kv, int S_k, int d
     return bytes + rows * sizeof(float2);
 }
 
-apex_status apex_attn_decode_ex(const void *q, const void *k_cache, const void *v_cache, void *out, int B, int H_q,
-                                int H_kv, int S_k, int d_h, const apex_attn_options *opt, void *workspace,
-                                size_t workspace_bytes, apex_stream_t stream)
+// Decode of the plain block (d_qk = d_v = d_rope = d_h) or of decoupled-RoPE
+// attention (d_qk = d_v + d_rope); argument checks of the callers done.
+apex_status decode_launch(const void *q, const void *k_cache, const void *v_cache, void *out, int B, int H_q,
+                          int H_kv, int S_k, int d_qk, int d_v, int d_rope, const apex_attn_options *opt,
+                          const RopeFreq &f, void *workspace, size_t workspace_bytes, apex_stream_t stream)
 {
-    if (!q || !k_cache || !v_cache || !out || !workspace || !opt) return APEX_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
-        return APEX_ERR_INVALID_ARG;
-    RopeFreq f;
-    if (!freq_of(*opt, &f)) return APEX_ERR_INVALID_ARG;
-    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, f.base);
-    if (s != APEX_OK) return s;
     const int q_pos = opt->q_pos, window = opt->window, P = opt->prefix_len;
     if (q_pos < 0 || q_pos >= S_k) return APEX_ERR_INVALID_ARG;
     if (P < 0 || P > S_k) return APEX_ERR_INVALID_ARG;
-    const size_t need = apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_h);
+    const size_t need = apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_v);
     if (workspace_bytes < need) return APEX_ERR_INVALID_ARG;
 
     int dev;
     DeviceState *st = current_state(&dev);
     if (!st) return APEX_ERR_CUDA;
     std::lock_guard<std::mutex> lk(st->mu);
-    s = init_device(*st, dev);
+    apex_status s = init_device(*st, dev);
     if (s != APEX_OK) return s;
     RopeTableView tv;
-    s = get_table(*st, d_h, f, S_k, &tv);
+    s = get_table(*st, d_rope, f, S_k, &tv);
     if (s != APEX_OK) return s;
 
     DecodeLaunch L;
     memset(&L, 0, sizeof L);
     const int units = B * H_kv;
-    if (!make_map(&L.tm_k, k_cache, d_h, S_k, units, kDecodeKeysPerStage, 1) ||
-        !make_map(&L.tm_v, v_cache, d_h, S_k, units, kDecodeKeysPerStage, 1))
+    if (!make_map(&L.tm_k, k_cache, d_qk, S_k, units, kDecodeKeysPerStage, 1) ||
+        !make_map(&L.tm_v, v_cache, d_v, S_k, units, kDecodeKeysPerStage, 1))
         return APEX_ERR_CUDA;
     DecodeParams &p = L.p;
     p.q = static_cast<const uint16_t *>(q);
     p.out = static_cast<uint16_t *>(out);
     const int ns_cap = decode_split_cap(units, max_stages_for(S_k));
     p.ws_o = static_cast<float *>(workspace);
-    size_t o_bytes = (size_t)B * H_q * ns_cap * d_h * sizeof(float);
+    size_t o_bytes = (size_t)B * H_q * ns_cap * d_v * sizeof(float);
     o_bytes = (o_bytes + 15) & ~size_t(15);
     p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + o_bytes);
     p.rope = tv;
@@ -359,7 +354,9 @@ apex_status apex_attn_decode_ex(const void *q, const void *k_cache, const void *
     p.H_kv = H_kv;
     p.G = H_q / H_kv;
     p.S_k = S_k;
-    p.d_h = d_h;
+    p.d_h = d_qk;
+    p.d_v = d_v;
+    p.d_rope = d_rope;
     p.q_pos = q_pos;
     // visible keys (Part 2, §10.2; a query inside the prefix sees the whole prefix, §11.1)
     if (q_pos < P) {
@@ -371,16 +368,48 @@ apex_status apex_attn_decode_ex(const void *q, const void *k_cache, const void *
     }
     p.stage0 = p.k_lo / kDecodeKeysPerStage;
     p.n_stages = p.k_hi / kDecodeKeysPerStage - p.stage0 + 1;
-    const int capacity = decode_ctas_per_sm(d_h, p.G) * st->sm_count;
+    const int capacity = decode_ctas_per_sm(d_qk, d_v, p.G) * st->sm_count;
     SplitPlan plan = plan_decode(units, p.n_stages, capacity);
     p.n_split = plan.n_split;
     p.stages_per_split = plan.stages_per_split;
     p.n_items = units * p.n_split;
-    p.scale_log2 = (float)(1.4426950408889634 * score_temperature(f) / sqrt((double)d_h));
+    p.scale_log2 = (float)(1.4426950408889634 * score_temperature(f) / sqrt((double)d_qk));
     L.grid = std::min(p.n_items, capacity);
     if (launch_decode(L, opt->keys_prerotated != 0, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return APEX_ERR_CUDA;
     return APEX_OK;
+}
+
+apex_status apex_attn_decode_ex(const void *q, const void *k_cache, const void *v_cache, void *out, int B, int H_q,
+                                int H_kv, int S_k, int d_h, const apex_attn_options *opt, void *workspace,
+                                size_t workspace_bytes, apex_stream_t stream)
+{
+    if (!q || !k_cache || !v_cache || !out || !workspace || !opt) return APEX_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
+        return APEX_ERR_INVALID_ARG;
+    RopeFreq f;
+    if (!freq_of(*opt, &f)) return APEX_ERR_INVALID_ARG;
+    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, f.base);
+    if (s != APEX_OK) return s;
+    return decode_launch(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, d_h, d_h, opt, f, workspace,
+                         workspace_bytes, stream);
+}
+
+apex_status apex_attn_mla_decode(const void *q, const void *k_cache, const void *v_cache, void *out, int B, int H_q,
+                                 int H_kv, int S_k, int d_h, int d_r, const apex_attn_options *opt, void *workspace,
+                                 size_t workspace_bytes, apex_stream_t stream)
+{
+    if (!q || !k_cache || !v_cache || !out || !workspace || !opt) return APEX_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
+        return APEX_ERR_INVALID_ARG;
+    if (d_r <= 0 || (d_r & 1)) return APEX_ERR_INVALID_ARG;
+    RopeFreq f;
+    if (!freq_of(*opt, &f)) return APEX_ERR_INVALID_ARG;
+    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, f.base);
+    if (s != APEX_OK) return s;
+    if (d_h != 128 || d_r != 64) return APEX_ERR_UNSUPPORTED;
+    return decode_launch(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h + d_r, d_h, d_r, opt, f, workspace,
+                         workspace_bytes, stream);
 }
 
 apex_status apex_attn_decode(const void *q, const void *k_cache, const void *v_cache, void *out, int B, int H_q,

@@ -22,6 +22,11 @@
 // At the end of an item the four warps merge their (max, sum, output) states
 // in shared memory and write one partial per (b, h, split).  A second kernel
 // merges the splits with a log-sum-exp reduction over warp shuffles.
+//
+// Query / key rows hold DQK entries, value / output rows DV; RoPE turns the
+// trailing DR entries of the query and key rows (DQK = DV = DR for the plain
+// block; DQK = DV + DR for decoupled RoPE, Part 2, §9.3, where the leading DV
+// entries -- the content part -- are used as they are).
 #include <math.h>
 
 #include "device_common.cuh"
@@ -35,14 +40,16 @@ constexpr int kBoxBytes = kKeys * 128;      // [64 keys][64 dims] bf16
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
-template <int D, int NT>
+template <int DQK, int DV, int NT>
 struct DecodeCfg {
-    static constexpr int kBoxes = D / 64;
-    static constexpr int kKBytes = kBoxes * kBoxBytes;
-    static constexpr int kQpRow = 2 * D + 16;  // padded row of the rotated queries
+    static constexpr int kKBoxes = DQK / 64;
+    static constexpr int kVBoxes = DV / 64;
+    static constexpr int kKBytes = kKBoxes * kBoxBytes;
+    static constexpr int kVBytes = kVBoxes * kBoxBytes;
+    static constexpr int kQpRow = 2 * DQK + 16;  // padded row of the rotated queries
     static constexpr int kQpBytes = 8 * NT * kQpRow;
-    static constexpr int kStageBytes = 2 * kKBytes + ((kQpBytes + 1023) / 1024) * 1024;
-    static constexpr int kRedFloats = 8 * NT * (2 + D);  // per warp: m, l, O[q][D]
+    static constexpr int kStageBytes = kKBytes + kVBytes + ((kQpBytes + 1023) / 1024) * 1024;
+    static constexpr int kRedFloats = 8 * NT * (2 + DV);  // per warp: m, l, O[q][DV]
     static constexpr int kRedOff = kStages * kStageBytes;
     static constexpr int kBarOff = kRedOff + kConsumerWarps * kRedFloats * 4;
     static constexpr int kSmemBytes = kBarOff + 2 * kStages * 8 + 1024;  // + alignment slack
@@ -55,12 +62,13 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 
 // PREROT: the cached keys already hold RoPE(k_j, j); the query is rotated to
 // its absolute position and the keys are used as they are.
-template <int D, int NT, bool PREROT>
+template <int DQK, int DV, int DR, int NT, bool PREROT>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const DecodeParams p)
 {
-    using C = DecodeCfg<D, NT>;
+    using C = DecodeCfg<DQK, DV, NT>;
+    static_assert(DQK == DV + DR || (DQK == DV && DR == DQK), "row split");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const uint32_t sbase = smem_u32(smem);
@@ -78,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // rows of the rotated-query area beyond G must read as zero
     for (int i = threadIdx.x; i < kStages * C::kQpBytes / 4; i += kThreads) {
         const int s = i / (C::kQpBytes / 4), w = i % (C::kQpBytes / 4);
-        reinterpret_cast<uint32_t *>(smem + s * C::kStageBytes + 2 * C::kKBytes)[w] = 0u;
+        reinterpret_cast<uint32_t *>(smem + s * C::kStageBytes + C::kKBytes + C::kVBytes)[w] = 0u;
     }
     __syncthreads();
 
@@ -88,7 +96,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
         }
-        constexpr int kPairs = D / 2;
+        constexpr int kPairs = DQK / 2;            // pairs of a query row
+        constexpr int kCPairs = (DQK - DR) / 2;    // pairs of its content part (not rotated)
+        constexpr int kRPairs = DR / 2;            // pairs of its rope part (table row length)
         constexpr int kPPL = (8 * NT * kPairs + 31) / 32;  // query pairs per lane
         const int n_pairs = p.G * kPairs;
         int it = 0;
@@ -105,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (pi < n_pairs) {
                     const int qi = pi / kPairs, i = pi % kPairs;
                     const uint32_t w = *reinterpret_cast<const uint32_t *>(
-                        p.q + ((size_t)(unit * p.G + qi) * D + 2 * i));
+                        p.q + ((size_t)(unit * p.G + qi) * DQK + 2 * i));
                     qv[k] = make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w));
                 }
             }
@@ -117,31 +127,37 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint32_t kdst = sbase + slot * C::kStageBytes;
                 const uint32_t vdst = kdst + C::kKBytes;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(bar_full + 8 * slot, 2 * C::kKBytes);
+                    mbar_arrive_expect_tx(bar_full + 8 * slot, C::kKBytes + C::kVBytes);
 #pragma unroll
-                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                    for (int bx = 0; bx < C::kKBoxes; ++bx)
                         tma_load_3d(kdst + bx * kBoxBytes, &tm_k, bar_full + 8 * slot, 64 * bx, j0, unit);
 #pragma unroll
-                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                    for (int bx = 0; bx < C::kVBoxes; ++bx)
                         tma_load_3d(vdst + bx * kBoxBytes, &tm_v, bar_full + 8 * slot, 64 * bx, j0, unit);
                 }
                 // Q' = R(q_pos - j0) q (Part 1, §4.2 rotation of each interleaved pair);
                 // a query inside a prefix can see keys after it: R(-a) = (cos a, -sin a).
                 // With pre-rotated keys, Q' = R(q_pos) q.
                 const int delta = PREROT ? p.q_pos : p.q_pos - j0;
-                const float2 *cs = p.rope.cs + (size_t)(delta < 0 ? -delta : delta) * kPairs;
+                const float2 *cs = p.rope.cs + (size_t)(delta < 0 ? -delta : delta) * kRPairs;
                 const float sgn = delta < 0 ? -1.f : 1.f;
-                uint8_t *qp = smem + slot * C::kStageBytes + 2 * C::kKBytes;
+                uint8_t *qp = smem + slot * C::kStageBytes + C::kKBytes + C::kVBytes;
 #pragma unroll
                 for (int k = 0; k < kPPL; ++k) {
                     const int pi = lane + 32 * k;
                     if (pi < n_pairs) {
                         const int qi = pi / kPairs, i = pi % kPairs;
-                        const float2 c0 = __ldg(cs + i);
-                        const float2 c = make_float2(c0.x, sgn * c0.y);
-                        const float y0 = fmaf(qv[k].x, c.x, -qv[k].y * c.y);
-                        const float y1 = fmaf(qv[k].x, c.y, qv[k].y * c.x);
-                        *reinterpret_cast<uint32_t *>(qp + qi * C::kQpRow + 4 * i) = pack_bf16x2(y0, y1);
+                        uint32_t word;
+                        if (kCPairs > 0 && i < kCPairs) {
+                            word = pack_bf16x2(qv[k].x, qv[k].y);  // content: exact bf16 copy
+                        } else {
+                            const float2 c0 = __ldg(cs + (i - kCPairs));
+                            const float2 c = make_float2(c0.x, sgn * c0.y);
+                            const float y0 = fmaf(qv[k].x, c.x, -qv[k].y * c.y);
+                            const float y1 = fmaf(qv[k].x, c.y, qv[k].y * c.x);
+                            word = pack_bf16x2(y0, y1);
+                        }
+                        *reinterpret_cast<uint32_t *>(qp + qi * C::kQpRow + 4 * i) = word;
                     }
                 }
                 __syncwarp();
@@ -153,19 +169,20 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ---------------------------------------------------------------- consumers
     const int g = lane >> 2, t = lane & 3;
-    constexpr int kPairs = D / 2;
+    constexpr int kRPairs = DR / 2;              // table row length
+    constexpr int kRopeStep0 = (DQK - DR) / 16;  // first k-step of the rope part
     // cos/sin of the key offsets this thread rotates: rows r0 = 16w+g, r1 = r0+8;
-    // in k-step s the pairs 8s+t (bits 0..7 of the step) and 8s+4+t.
-    float2 csk[2][D / 8];
+    // in rope k-step sr the rope pairs 8sr+t (bits 0..7 of the step) and 8sr+4+t.
+    float2 csk[2][DR / 8];
     {
         const int r0 = 16 * warp + g;
 #pragma unroll
-        for (int s = 0; s < D / 16; ++s)
+        for (int sr = 0; sr < DR / 16; ++sr)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int pair = 8 * s + 4 * h + t;
-                csk[0][2 * s + h] = __ldg(p.rope.cs + (size_t)r0 * kPairs + pair);
-                csk[1][2 * s + h] = __ldg(p.rope.cs + (size_t)(r0 + 8) * kPairs + pair);
+                const int pair = 8 * sr + 4 * h + t;
+                csk[0][2 * sr + h] = __ldg(p.rope.cs + (size_t)r0 * kRPairs + pair);
+                csk[1][2 * sr + h] = __ldg(p.rope.cs + (size_t)(r0 + 8) * kRPairs + pair);
             }
     }
     float *red_all = reinterpret_cast<float *>(smem + C::kRedOff);
@@ -178,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int s_end = min(p.stage0 + p.n_stages, s_begin + p.stages_per_split);
 
         float m_run[NT][2], l_run[NT][2];
-        float acc_o[D / 16][NT][4];
+        float acc_o[DV / 16][NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -187,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 l_run[nt][c] = 0.f;
             }
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt)
+        for (int mt = 0; mt < DV / 16; ++mt)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -199,16 +216,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int j0 = st * kKeys;
             const uint32_t kb = sbase + slot * C::kStageBytes;
             const uint32_t vb = kb + C::kKBytes;
-            const uint32_t qp = vb + C::kKBytes;
+            const uint32_t qp = vb + C::kVBytes;
 
-            // S^T[16 keys x 8NT queries] = K'[16 x D] . Q'^T[D x 8NT]
+            // S^T[16 keys x 8NT queries] = K'[16 x DQK] . Q'^T[DQK x 8NT]
             float acc_s[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc_s[nt][e] = 0.f;
 #pragma unroll
-            for (int s2 = 0; s2 < D / 32; ++s2) {
+            for (int s2 = 0; s2 < DQK / 32; ++s2) {
                 uint32_t bq[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -220,11 +237,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const uint32_t chunk = 2 * s + (lane >> 4);
                     uint32_t a[4];
                     ldmatrix_x4(a, kb + (chunk >> 3) * kBoxBytes + swz128(row, chunk & 7));
-                    if (!PREROT) {
-                        a[0] = rope_pair_bf16(a[0], csk[0][2 * s].x, csk[0][2 * s].y);
-                        a[1] = rope_pair_bf16(a[1], csk[1][2 * s].x, csk[1][2 * s].y);
-                        a[2] = rope_pair_bf16(a[2], csk[0][2 * s + 1].x, csk[0][2 * s + 1].y);
-                        a[3] = rope_pair_bf16(a[3], csk[1][2 * s + 1].x, csk[1][2 * s + 1].y);
+                    if (!PREROT && s >= kRopeStep0) {
+                        const int sr = s - kRopeStep0;
+                        a[0] = rope_pair_bf16(a[0], csk[0][2 * sr].x, csk[0][2 * sr].y);
+                        a[1] = rope_pair_bf16(a[1], csk[1][2 * sr].x, csk[1][2 * sr].y);
+                        a[2] = rope_pair_bf16(a[2], csk[0][2 * sr + 1].x, csk[0][2 * sr + 1].y);
+                        a[3] = rope_pair_bf16(a[3], csk[1][2 * sr + 1].x, csk[1][2 * sr + 1].y);
                     }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc_s[nt], a, bq[nt][2 * h2], bq[nt][2 * h2 + 1]);
@@ -256,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     l_run[nt][c] = l_run[nt][c] * alpha + pv[c] + pv[c + 2];
                     m_run[nt][c] = m_new;
 #pragma unroll
-                    for (int mt = 0; mt < D / 16; ++mt) {
+                    for (int mt = 0; mt < DV / 16; ++mt) {
                         acc_o[mt][nt][c] *= alpha;
                         acc_o[mt][nt][c + 2] *= alpha;
                     }
@@ -266,9 +284,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 bp[nt][1] = movmatrix_trans(pack_bf16x2(pv[2], pv[3]));
             }
 
-            // O^T[D x 8NT] += V^T[D x 16 keys] . P^T[16 keys x 8NT]
+            // O^T[DV x 8NT] += V^T[DV x 16 keys] . P^T[16 keys x 8NT]
 #pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
+            for (int mt = 0; mt < DV / 16; ++mt) {
                 const uint32_t row = 16 * warp + (lane & 7) + (lane >> 4) * 8;
                 const uint32_t chunk = 2 * mt + ((lane >> 3) & 1);
                 uint32_t a[4];
@@ -295,14 +313,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                     red[8 * NT + qc] = l;
                 }
 #pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt) {
-                    red[16 * NT + qc * D + 16 * mt + g] = acc_o[mt][nt][c];
-                    red[16 * NT + qc * D + 16 * mt + g + 8] = acc_o[mt][nt][c + 2];
+                for (int mt = 0; mt < DV / 16; ++mt) {
+                    red[16 * NT + qc * DV + 16 * mt + g] = acc_o[mt][nt][c];
+                    red[16 * NT + qc * DV + 16 * mt + g + 8] = acc_o[mt][nt][c + 2];
                 }
             }
         named_bar_sync(1, kConsumerWarps * 32);
-        for (int idx = threadIdx.x; idx < p.G * D; idx += kConsumerWarps * 32) {
-            const int qc = idx / D, e = idx % D;
+        for (int idx = threadIdx.x; idx < p.G * DV; idx += kConsumerWarps * 32) {
+            const int qc = idx / DV, e = idx % DV;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_all[w * C::kRedFloats + qc]);
@@ -314,10 +332,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const float mw = rw[qc];
                 const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
                 L += f * rw[8 * NT + qc];
-                O += f * rw[16 * NT + qc * D + e];
+                O += f * rw[16 * NT + qc * DV + e];
             }
             const size_t slot_idx = (size_t)(unit * p.G + qc) * p.n_split + split;
-            p.ws_o[slot_idx * D + e] = O;
+            p.ws_o[slot_idx * DV + e] = O;
             if (e == 0) p.ws_ml[slot_idx] = make_float2(M, L);
         }
         named_bar_sync(1, kConsumerWarps * 32);
@@ -365,18 +383,18 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
     for (int e = 0; e < E / 2; ++e) dst[e] = packed[e];
 }
 
-template <int D, int NT, bool PREROT>
+template <int DQK, int DV, int DR, int NT, bool PREROT>
 cudaError_t launch_t(const DecodeLaunch &L, cudaStream_t stream)
 {
-    using C = DecodeCfg<D, NT>;
-    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<D, NT, PREROT>,
+    using C = DecodeCfg<DQK, DV, NT>;
+    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<DQK, DV, DR, NT, PREROT>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
-    decode_split_kernel<D, NT, PREROT><<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tm_k, L.tm_v, L.p);
+    decode_split_kernel<DQK, DV, DR, NT, PREROT><<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tm_k, L.tm_v, L.p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const int rows = L.p.B * L.p.H_q;
-    decode_combine_kernel<D><<<(rows + 3) / 4, 128, 0, stream>>>(L.p);
+    decode_combine_kernel<DV><<<(rows + 3) / 4, 128, 0, stream>>>(L.p);
     return cudaGetLastError();
 }
 
@@ -384,8 +402,13 @@ template <bool PREROT>
 cudaError_t dispatch(const DecodeLaunch &L, cudaStream_t stream)
 {
     const bool wide = L.p.G > 8;
-    if (L.p.d_h == 128) return wide ? launch_t<128, 2, PREROT>(L, stream) : launch_t<128, 1, PREROT>(L, stream);
-    if (L.p.d_h == 64) return wide ? launch_t<64, 2, PREROT>(L, stream) : launch_t<64, 1, PREROT>(L, stream);
+    const int dqk = L.p.d_h, dv = L.p.d_v, dr = L.p.d_rope;
+    if (dqk == 128 && dv == 128 && dr == 128)
+        return wide ? launch_t<128, 128, 128, 2, PREROT>(L, stream) : launch_t<128, 128, 128, 1, PREROT>(L, stream);
+    if (dqk == 64 && dv == 64 && dr == 64)
+        return wide ? launch_t<64, 64, 64, 2, PREROT>(L, stream) : launch_t<64, 64, 64, 1, PREROT>(L, stream);
+    if (dqk == 192 && dv == 128 && dr == 64)
+        return wide ? launch_t<192, 128, 64, 2, PREROT>(L, stream) : launch_t<192, 128, 64, 1, PREROT>(L, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -396,11 +419,20 @@ cudaError_t launch_decode(const DecodeLaunch &L, bool keys_prerotated, cudaStrea
     return keys_prerotated ? dispatch<true>(L, stream) : dispatch<false>(L, stream);
 }
 
-int decode_ctas_per_sm(int d_h, int G)
+// Resident split-kernel CTAs per SM (the shared-memory footprint decides).
+int decode_ctas_per_sm(int d_qk, int d_v, int G)
 {
-    (void)d_h;
-    (void)G;
-    return 2;
+    const bool wide = G > 8;
+    int bytes = 0;
+    if (d_qk == 192 && d_v == 128)
+        bytes = wide ? DecodeCfg<192, 128, 2>::kSmemBytes : DecodeCfg<192, 128, 1>::kSmemBytes;
+    else if (d_qk == 128)
+        bytes = wide ? DecodeCfg<128, 128, 2>::kSmemBytes : DecodeCfg<128, 128, 1>::kSmemBytes;
+    else
+        bytes = wide ? DecodeCfg<64, 64, 2>::kSmemBytes : DecodeCfg<64, 64, 1>::kSmemBytes;
+    // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA
+    const int n = (228 * 1024) / (bytes + 1024);
+    return n < 1 ? 1 : (n > 2 ? 2 : n);
 }
 
 }  // namespace apex

@@ -167,6 +167,8 @@ extern "C" apex_status apex_attn_decode_noalloc(const void *q, const void *k_cac
     p.G = G;
     p.S_k = S_k;
     p.d_h = d_h;
+    p.d_v = d_h;
+    p.d_rope = d_h;
     p.q_pos = q_pos;
     p.k_lo = (window > 0) ? std::max(0, q_pos - window + 1) : 0;
     p.k_hi = q_pos;
@@ -176,7 +178,7 @@ extern "C" apex_status apex_attn_decode_noalloc(const void *q, const void *k_cac
     // splits: as many as the modelled time prefers, within what g_scratch holds
     int cap = (int)std::min<long>(std::max(1l, 32768l / units), (long)p.n_stages);
     while (cap > 1 && partial_bytes(B, H_q, cap, d_h) > kScratchBytes) --cap;
-    const int capacity = decode_ctas_per_sm(d_h, G) * st.sm_count;
+    const int capacity = decode_ctas_per_sm(d_h, d_h, G) * st.sm_count;
     int best_ns = 1, best_sps = p.n_stages;
     double best_cost = 1e300;
     for (int ns = 1; ns <= cap; ++ns) {

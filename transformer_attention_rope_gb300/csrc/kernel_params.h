@@ -44,6 +44,8 @@ struct DecodeParams {
     int stages_per_split;   // last split may have fewer
     int n_items;            // B * H_kv * n_split
     float scale_log2;       // log2(e) / sqrt(d_h)
+    int d_v;                // value / output row length (d_h for the plain block)
+    int d_rope;             // trailing q / k entries RoPE turns (d_h for the plain block)
 };
 
 struct DecodeLaunch {
@@ -54,7 +56,7 @@ struct DecodeLaunch {
 
 // keys_prerotated selects the variant that uses the cached keys as they are
 cudaError_t launch_decode(const DecodeLaunch &L, bool keys_prerotated, cudaStream_t stream);
-int decode_ctas_per_sm(int d_h, int G);
+int decode_ctas_per_sm(int d_qk, int d_v, int G);
 
 // ----------------------------------------------------------------- prefill
 struct PrefillParams {

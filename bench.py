@@ -72,8 +72,9 @@ def prefill_flops(w, prefix_len=0):
 
 
 def decode_kv_bytes(w, prefix_len=0):
+    """K and V bytes a decode call must read: key rows of d_h + d_r, value rows of d_h entries."""
     lo, hi = visible_range(w.q_pos0, w.window, prefix_len)
-    return 2.0 * w.B * w.H_kv * (hi - lo + 1) * w.d_h * 2
+    return 2.0 * w.B * w.H_kv * (hi - lo + 1) * (2 * w.d_h + w.d_r)
 
 
 # --feature: the options of the block beyond the plain path, as keyword arguments
@@ -87,11 +88,11 @@ FEATURES = {
 }
 
 
-def rank_workloads(rank, prefill_name=PREFILL, decode_batch=None):
+def rank_workloads(rank, prefill_name=PREFILL, decode_batch=None, decode_name=DECODE):
     """The step's two workloads for one rank: same shapes on every rank, seeds
     offset by rank (independent problems, no data shared between ranks)."""
     from transformer_attention_rope_gb300 import inputs as inp
-    wp, wd = inp.WORKLOADS[prefill_name], inp.WORKLOADS[DECODE]
+    wp, wd = inp.WORKLOADS[prefill_name], inp.WORKLOADS[decode_name]
     if decode_batch:
         wd = dataclasses.replace(wd, B=decode_batch)
     return (dataclasses.replace(wp, seed=wp.seed + 1000 * rank),
@@ -220,11 +221,14 @@ def oracle_sample_prefill(w, q, k, v, budget_rows, batches=1):
 def oracle_sample_decode(w, q, k, v, n_batch):
     import oracle
     t0 = time.perf_counter()
-    oracle.attn(q[:n_batch], k[:n_batch], v[:n_batch], window=w.window, q_pos0=w.q_pos0)
+    if w.d_r:
+        oracle.mla_attn(q[:n_batch], k[:n_batch], v[:n_batch], w.d_r, window=w.window, q_pos0=w.q_pos0)
+    else:
+        oracle.attn(q[:n_batch], k[:n_batch], v[:n_batch], window=w.window, q_pos0=w.q_pos0)
     dt = time.perf_counter() - t0
     m = w.q_pos0
     lo = max(0, m - w.window + 1) if w.window > 0 else 0
-    nbytes = 2.0 * n_batch * w.H_kv * (m - lo + 1) * w.d_h * 2
+    nbytes = 2.0 * n_batch * w.H_kv * (m - lo + 1) * (2 * w.d_h + w.d_r)
     return nbytes, dt, "decode: %d of %d sequences, full cache" % (n_batch, w.B)
 
 
@@ -302,7 +306,7 @@ def run_ours(args):
         pg = dist
     apex.load_library()
 
-    wp, wd = rank_workloads(rank, args.prefill_workload, args.decode_batch)
+    wp, wd = rank_workloads(rank, args.prefill_workload, args.decode_batch, args.decode_workload)
     do_pre, do_dec = args.part in ("all", "prefill"), args.part in ("all", "decode")
     stream = torch.cuda.current_stream()
 
@@ -316,15 +320,15 @@ def run_ours(args):
     if do_dec:
         din = inp.workload_inputs(dataclasses.replace(wd, S_q=1), pin=True)
         dq, dk, dv = (t.to(dev, non_blocking=True) for t in din)
-        dout = torch.empty_like(dq)
+        dout = torch.empty((wd.B, wd.H_q, 1, wd.d_h), dtype=torch.bfloat16, device=dev)
         dout_h = torch.empty(dout.shape, dtype=dout.dtype, pin_memory=True)
         ws = torch.empty(apex.decode_workspace_bytes(wd.B, wd.H_q, wd.H_kv, wd.S_k, wd.d_h), dtype=torch.uint8,
                          device=dev)
-        apex.apex_attn_rope_reserve(wd.S_k, wd.d_h, wd.rope_base)
+        apex.apex_attn_rope_reserve(wd.S_k, wd.d_r or wd.d_h, wd.rope_base)
     torch.cuda.synchronize()
 
     feat = FEATURES[args.feature]
-    if wp.d_r and feat.get("keys_prerotated"):
+    if (wp.d_r or wd.d_r) and feat.get("keys_prerotated"):
         raise SystemExit("--feature prerotated rotates whole key rows; not defined for the decoupled-RoPE workload")
     if feat.get("keys_prerotated"):
         # the caches hold RoPE(k_j, j): rotate the keys once, outside the timing
@@ -342,8 +346,12 @@ def run_ours(args):
             apex.fwd(pq, pk, pv, window=wp.window, q_pos0=wp.q_pos0, rope_base=wp.rope_base, out=pout, **feat)
 
     def decode():
-        apex.decode(dq, dk, dv, wd.q_pos0, window=wd.window, rope_base=wd.rope_base, out=dout, workspace=ws,
-                    **feat)
+        if wd.d_r:
+            apex.mla_decode(dq, dk, dv, wd.q_pos0, wd.d_r, window=wd.window, rope_base=wd.rope_base, out=dout,
+                            workspace=ws, **feat)
+        else:
+            apex.decode(dq, dk, dv, wd.q_pos0, window=wd.window, rope_base=wd.rope_base, out=dout, workspace=ws,
+                        **feat)
 
     warm = max(3, args.warmup)
     for _ in range(warm):
@@ -432,8 +440,9 @@ def run_ours(args):
                 wp.name, wp.B, wp.H_q, wp.H_kv, wp.S_q, wp.d_h, ("+%d decoupled RoPE" % wp.d_r) if wp.d_r else "",
                 wp.window))
         if do_dec:
-            desc.append("decode (B%d Hq%d Hkv%d Sk%d d%d q_pos %d)" % (wd.B, wd.H_q, wd.H_kv, wd.S_k, wd.d_h,
-                                                                        wd.q_pos0))
+            desc.append("decode %s(B%d Hq%d Hkv%d Sk%d d%d%s q_pos %d)" % (
+                (wd.name + " ") if wd.d_r else "", wd.B, wd.H_q, wd.H_kv, wd.S_k, wd.d_h,
+                ("+%d decoupled RoPE" % wd.d_r) if wd.d_r else "", wd.q_pos0))
         if args.feature != "none":
             desc.append("feature %s %s" % (args.feature, json.dumps(feat)))
         line["config"] = {
@@ -525,6 +534,7 @@ def main():
     ap.add_argument("--part", choices=["all", "prefill", "decode"], default="all",
                     help="run only one of the two calls per step (profiling)")
     ap.add_argument("--prefill-workload", choices=["tiny", "gqa", "wide", "long", "mla"], default=PREFILL)
+    ap.add_argument("--decode-workload", choices=["decode", "mla_decode"], default=DECODE)
     ap.add_argument("--feature", choices=sorted(FEATURES), default="none",
                     help="run the step with one of the block's options")
     ap.add_argument("--decode-batch", type=int, default=None,

@@ -62,6 +62,8 @@ WORKLOADS = {
     "decode": Workload("decode", 64, 32, 8, 1, 32768, 128, 0, 32767, 4, decode=True),
     # global-layer prefill of multi-head latent attention with a 64-entry decoupled RoPE part
     "mla": Workload("mla", 1, 128, 8, 8192, 8192, 128, 0, 0, 5, d_r=64),
+    # the decode cache shape with decoupled-RoPE key rows (128 + 64 entries)
+    "mla_decode": Workload("mla_decode", 64, 32, 8, 1, 32768, 128, 0, 32767, 6, decode=True, d_r=64),
 }
 
 

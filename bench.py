@@ -476,7 +476,7 @@ def run_ours(args):
             line["roofline_decode"] = {"kernel": "decode_split_kernel (+ its combine kernel, timed together)",
                                        "bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"],
                                        "unit": "GB/s", "frac": dec_achieved / peaks["hbm_gbs"],
-                                       "traffic": traffic.get("decode"), "peak_source": peaks["source"]}
+                                       "traffic": traffic.get(wd.name), "peak_source": peaks["source"]}
             e2e.update({"decode_value": world * K * kvb / te_dec / 1e9, "decode_unit": "GB/s"})
             if not do_pre:
                 line["value"], line["unit"] = line["decode"]["value"], "GB/s"

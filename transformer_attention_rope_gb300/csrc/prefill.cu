@@ -35,9 +35,9 @@ constexpr int kThreads = 16 * 32;
 // refuses to launch unless 128 x (2 kRegsSoftmax + kRegsRope + kRegsCtl) fits
 // in what the block was actually launched with.
 constexpr int kLaunchRegs = 128;
-constexpr int kRegsSoftmax = 168;
-constexpr int kRegsRope = 88;
-constexpr int kRegsCtl = 88;
+constexpr int kRegsSoftmax = 176;
+constexpr int kRegsRope = 80;
+constexpr int kRegsCtl = 80;
 static_assert(128 * (2 * kRegsSoftmax + kRegsRope + kRegsCtl) <= kThreads * kLaunchRegs, "register split");
 constexpr int kWarpRope = 8;
 constexpr int kWarpTma = 12;
@@ -317,22 +317,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+            // One descriptor per operand and call, stepped by adding the k-step's
+            // offset (>> 4) to its address field; the empty asm keeps the base a
+            // runtime value, so the compiler does not precompute (and keep live)
+            // the descriptors of every tile and stage.
+            auto desc_base = [&](uint32_t addr, uint32_t lbo) -> uint64_t {
+                uint64_t d = smem_desc_sw128(addr, lbo, 1024);
+                asm volatile("" : "+l"(d));
+                return d;
+            };
             auto issue_qk = [&](int t, int ks) {
-                const uint32_t qa = sb + C::kQOff + t * C::kTile;
-                const uint32_t kb = sb + C::kKOff + ks * C::kTile;
+                const uint64_t da = desc_base(sb + C::kQOff + t * C::kTile, 16);
+                const uint64_t db = desc_base(sb + C::kKOff + ks * C::kTile, 16);
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
-                    const uint32_t off = (s >> 2) * kBoxBytes + (s & 3) * 32;
-                    umma_ss(tmem + C::col_s(t), smem_desc_sw128(qa + off, 16, 1024),
-                            smem_desc_sw128(kb + off, 16, 1024), idesc_qk, s > 0 ? 1u : 0u);
+                    const uint64_t off = ((s >> 2) * kBoxBytes + (s & 3) * 32) >> 4;
+                    umma_ss(tmem + C::col_s(t), da + off, db + off, idesc_qk, s > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int vs, bool acc) {
-                const uint32_t vb = sb + C::kVOff + vs * C::kTile;
+                const uint64_t dv = desc_base(sb + C::kVOff + vs * C::kTile, kBoxBytes);
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 8 * s,
-                            smem_desc_sw128(vb + s * 2048, kBoxBytes, 1024), idesc_pv, (acc || s > 0) ? 1u : 0u);
+                    umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 8 * s, dv + (uint64_t)(s * 2048 >> 4), idesc_pv,
+                            (acc || s > 0) ? 1u : 0u);
             };
             int kc = 0;
             for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {

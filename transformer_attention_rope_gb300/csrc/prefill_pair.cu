@@ -39,9 +39,9 @@ constexpr int kWarpTma = 12;
 constexpr int kWarpMma = 13;
 constexpr int kWarpRelay = 14;
 constexpr int kLaunchRegs = 128;
-constexpr int kRegsSoftmax = 168;
+constexpr int kRegsSoftmax = 176;
 constexpr int kRegsRope = 88;
-constexpr int kRegsCtl = 88;
+constexpr int kRegsCtl = 72;
 static_assert(128 * (2 * kRegsSoftmax + kRegsRope + kRegsCtl) <= kThreads * kLaunchRegs, "register split");
 
 constexpr int kQBox = 128 * 128;  // [128 rows][64 dims]
@@ -417,21 +417,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (rank == 0 && lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(256, 128, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(256, 128, true);
+            // One descriptor per operand and call, stepped by adding the k-step's
+            // offset (>> 4) to its address field; the empty asm keeps the base a
+            // runtime value, so the compiler does not precompute (and keep live)
+            // the descriptors of every tile and stage.
+            auto desc_base = [&](uint32_t addr, uint32_t lbo) -> uint64_t {
+                uint64_t d = smem_desc_sw128(addr, lbo, 1024);
+                asm volatile("" : "+l"(d));
+                return d;
+            };
             auto issue_qk = [&](int t, int ks) {
-                const uint32_t qa = sb + kQOff + t * kQTile;
-                const uint32_t kb = sb + kKOff + ks * kKTile;
+                const uint64_t da = desc_base(sb + kQOff + t * kQTile, 16);
+                const uint64_t db = desc_base(sb + kKOff + ks * kKTile, 16);
 #pragma unroll
                 for (int s = 0; s < DQK / 16; ++s)
-                    mma_ss_pair(tmem + col_s(t), smem_desc_sw128(qa + (s >> 2) * kQBox + (s & 3) * 32, 16, 1024),
-                                smem_desc_sw128(kb + (s >> 2) * kKBox + (s & 3) * 32, 16, 1024), idesc_qk,
-                                s > 0 ? 1u : 0u);
+                    mma_ss_pair(tmem + col_s(t), da + (uint64_t)(((s >> 2) * kQBox + (s & 3) * 32) >> 4),
+                                db + (uint64_t)(((s >> 2) * kKBox + (s & 3) * 32) >> 4), idesc_qk, s > 0 ? 1u : 0u);
             };
             auto issue_pv = [&](int t, int vs, bool acc) {
-                const uint32_t vb = sb + kVOff + vs * kVTile;
+                const uint64_t dv = desc_base(sb + kVOff + vs * kVTile, kQBox);
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_ts_pair(tmem + col_o(t), tmem + col_s(t) + 8 * s, smem_desc_sw128(vb + s * 2048, kQBox, 1024),
-                                idesc_pv, (acc || s > 0) ? 1u : 0u);
+                    mma_ts_pair(tmem + col_o(t), tmem + col_s(t) + 8 * s, dv + (uint64_t)(s * 2048 >> 4), idesc_pv,
+                                (acc || s > 0) ? 1u : 0u);
             };
             int kc = 0;
             for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {

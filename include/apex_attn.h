@@ -153,6 +153,16 @@ apex_status apex_attn_decode_ex(const void *q, const void *k_cache, const void *
                                 size_t workspace_bytes, apex_stream_t stream);
 
 /*
+ * Diagnostic (the pages have no counterpart): launches one CTA whose bounded
+ * mbarrier wait -- the wait every kernel of this library uses -- can never
+ * complete.  After timeout_ms (1..5000, else APEX_ERR_INVALID_ARG) the wait
+ * gives up, records its code in the per-device status word and the kernel
+ * returns; apex_attn_device_status() then reports APEX_ERR_DEVICE_TIMEOUT
+ * (and clears it) and the context stays usable.  Asynchronous on `stream`.
+ */
+apex_status apex_attn_selftest_wait_timeout(int timeout_ms, apex_stream_t stream);
+
+/*
  * Decode of multi-head latent attention with decoupled RoPE (Part 2 §9.3):
  * one query per sequence against a cache of [content | rope part] keys.
  *

@@ -24,7 +24,8 @@ __all__ = [
     "ApexError", "library_path", "load_library", "apex_attn_fwd", "apex_attn_decode", "apex_attn_decode_noalloc",
     "apex_attn_decode_workspace_bytes", "apex_attn_rope_reserve", "apex_attn_device_status",
     "apex_attn_status_string", "apex_attn_fwd_ex", "apex_attn_decode_ex", "apex_attn_rope_keys",
-    "apex_attn_mla_fwd", "apex_attn_mla_decode", "Options", "fwd", "decode", "decode_workspace_bytes",
+    "apex_attn_mla_fwd", "apex_attn_mla_decode", "apex_attn_selftest_wait_timeout", "Options", "fwd", "decode",
+    "decode_workspace_bytes",
     "rope_keys", "mla_fwd", "mla_decode",
 ]
 
@@ -87,6 +88,8 @@ def load_library():
             lib.apex_attn_decode_workspace_bytes.restype = sz
             lib.apex_attn_rope_reserve.argtypes = [i32, i32, f32]
             lib.apex_attn_rope_reserve.restype = i32
+            lib.apex_attn_selftest_wait_timeout.argtypes = [i32, vp]
+            lib.apex_attn_selftest_wait_timeout.restype = i32
             lib.apex_attn_device_status.argtypes = []
             lib.apex_attn_device_status.restype = i32
             lib.apex_attn_status_string.argtypes = [i32]
@@ -150,6 +153,10 @@ def apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_h) -> int:
 
 def apex_attn_rope_reserve(max_pos, d_h, rope_base) -> int:
     return load_library().apex_attn_rope_reserve(max_pos, d_h, rope_base)
+
+
+def apex_attn_selftest_wait_timeout(timeout_ms, stream) -> int:
+    return load_library().apex_attn_selftest_wait_timeout(timeout_ms, stream)
 
 
 def apex_attn_device_status() -> int:

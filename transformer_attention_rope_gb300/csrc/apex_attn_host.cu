@@ -300,6 +300,20 @@ apex_status apex_attn_device_status(void)
     return APEX_ERR_DEVICE_TIMEOUT;
 }
 
+apex_status apex_attn_selftest_wait_timeout(int timeout_ms, apex_stream_t stream)
+{
+    if (timeout_ms < 1 || timeout_ms > 5000) return APEX_ERR_INVALID_ARG;
+    int dev;
+    DeviceState *st = current_state(&dev);
+    if (!st) return APEX_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(st->mu);
+    apex_status s = init_device(*st, dev);
+    if (s != APEX_OK) return s;
+    const WaitCtl wc{st->status, (uint64_t)timeout_ms * 1000000ull};
+    if (launch_wait_selftest(wc, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return APEX_ERR_CUDA;
+    return APEX_OK;
+}
+
 size_t apex_attn_decode_workspace_bytes(int B, int H_q, int H_kv, int S_k, int d_h)
 {
     if (check_common(B, H_q, H_kv, S_k, d_h, 10000.f) != APEX_OK) return 0;

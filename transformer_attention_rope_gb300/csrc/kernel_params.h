@@ -98,4 +98,8 @@ struct RopeKeysParams {
 
 cudaError_t launch_rope_keys(const RopeKeysParams &p, int sm_count, cudaStream_t stream);
 
+// ----------------------------------------------------------------- self-test
+// one CTA whose bounded mbarrier wait can never complete (reports kStatusWaitTimeout)
+cudaError_t launch_wait_selftest(const WaitCtl &wc, cudaStream_t stream);
+
 }  // namespace apex

@@ -459,12 +459,13 @@ def run_ours(args):
             line["prefill"] = {"value": line["value"], "unit": "TFLOP/s", "ms_per_call": pre_launch_s * 1e3,
                                "frac_of_bf16": pre_achieved / peaks["bf16_tflops"],
                                "frac_of_bf16_sustained": pre_achieved / peaks["bf16_tflops_sustained"]}
-            kname = "prefill_pair_kernel" if (wp.d_r or os.environ.get("APEX_ATTN_PREFILL") == "pair") \
-                else "prefill_kernel"
+            kname = "prefill_kernel" if (not wp.d_r and (wp.d_h != 128 or os.environ.get("APEX_ATTN_PREFILL")
+                                                                 == "single")) else "prefill_pair_kernel"
             line["roofline_prefill"] = {"kernel": kname, "bound": "tensor", "achieved": pre_achieved,
                                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                         "frac": pre_achieved / peaks["bf16_tflops"],
-                                        "traffic": traffic.get("prefill_" + wp.name),
+                                        "traffic": traffic.get("prefill_" + wp.name +
+                                                               ("_single" if kname == "prefill_kernel" else "")),
                                         "peak_source": peaks["source"] + " (burst)"}
             e2e.update({"value": world * K * flops / te_pre / 1e12, "unit": "TFLOP/s"})
         if do_dec:

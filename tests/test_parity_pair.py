@@ -1,6 +1,7 @@
-"""GPU parity of the CTA-pair prefill kernel (tcgen05 cta_group::2) on the plain
-block, selected per call with APEX_ATTN_PREFILL=pair: the same tolerance as the
-single-CTA kernel (max |err| <= 2e-2, mean |err| <= 2e-3)."""
+"""GPU parity of both prefill kernels for d_h = 128 on the plain block: the
+CTA-pair kernel (tcgen05 cta_group::2, the default) and the single-CTA kernel
+(APEX_ATTN_PREFILL=single, read at each call), same tolerance as everywhere
+(max |err| <= 2e-2, mean |err| <= 2e-3)."""
 import numpy as np
 import pytest
 import torch
@@ -23,6 +24,14 @@ def pair_kernel(monkeypatch):
     yield torch.device("cuda:0")
 
 
+@pytest.fixture(params=["pair", "single"])
+def either_kernel(request, monkeypatch):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    monkeypatch.setenv("APEX_ATTN_PREFILL", request.param)
+    yield torch.device("cuda:0")
+
+
 def _qkv(B, H_q, H_kv, S_q, S_k, d, seed):
     return (inputs.normal_bf16((B, H_q, S_q, d), seed, 0), inputs.normal_bf16((B, H_kv, S_k, d), seed, 1),
             inputs.normal_bf16((B, H_kv, S_k, d), seed, 2))
@@ -39,10 +48,10 @@ CASES = [  # B, H_q, H_kv, S_q, S_k, window, q_pos0, prefix
 
 
 @pytest.mark.parametrize("B,H_q,H_kv,S_q,S_k,window,q_pos0,prefix", CASES)
-def test_pair_prefill_matches_oracle(pair_kernel, B, H_q, H_kv, S_q, S_k, window, q_pos0, prefix):
+def test_prefill_kernels_match_oracle(either_kernel, B, H_q, H_kv, S_q, S_k, window, q_pos0, prefix):
+    dev = either_kernel
     q, k, v = _qkv(B, H_q, H_kv, S_q, S_k, 128, 1200 + S_q + window)
-    out = apex.fwd(q.to(pair_kernel), k.to(pair_kernel), v.to(pair_kernel), window=window, q_pos0=q_pos0,
-                   prefix_len=prefix)
+    out = apex.fwd(q.to(dev), k.to(dev), v.to(dev), window=window, q_pos0=q_pos0, prefix_len=prefix)
     torch.cuda.synchronize()
     ref = oracle.attn(q, k, v, window=window, q_pos0=q_pos0, prefix_len=prefix)
     e = np.abs(out.double().cpu().numpy() - ref)

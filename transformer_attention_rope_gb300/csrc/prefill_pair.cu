@@ -22,8 +22,9 @@
 //     multicast, so every CTA waits on local barriers only.
 //
 // Warps per CTA: 0-3 / 4-7 softmax + epilogue of tiles 0 / 1 (and their Q
-// RoPE), 8-11 K RoPE, 12 TMA producer, 13 MMA issuer (leader) / TMEM
-// allocation, 14 relays "V landed" to the leader, 15 idle.
+// RoPE), 8-11 K RoPE (their "K ready" arrival also vouches that the V tile of
+// the same index has landed, so the MMA thread has one wait less per tile),
+// 12 TMA producer, 13 MMA issuer (leader) / TMEM allocation, 14-15 idle.
 #include <math.h>
 
 #include "device_common.cuh"
@@ -37,7 +38,6 @@ constexpr int kThreads = 16 * 32;
 constexpr int kWarpRope = 8;
 constexpr int kWarpTma = 12;
 constexpr int kWarpMma = 13;
-constexpr int kWarpRelay = 14;
 constexpr int kLaunchRegs = 128;
 constexpr int kRegsSoftmax = 176;
 constexpr int kRegsRope = 88;
@@ -78,8 +78,7 @@ struct PairCfg {
     static constexpr int kBarKReady = kBarKFull + kKStages;     // [K]  leader: 8 warps
     static constexpr int kBarKEmpty = kBarKReady + kKStages;    // [K]  multicast commit
     static constexpr int kBarVFull = kBarKEmpty + kKStages;     // [V]  local TMA
-    static constexpr int kBarVReady = kBarVFull + kVStages;     // [V]  leader: 2 relays
-    static constexpr int kBarVEmpty = kBarVReady + kVStages;    // [V]  multicast commit
+    static constexpr int kBarVEmpty = kBarVFull + kVStages;     // [V]  multicast commit
     static constexpr int kNumBars = kBarVEmpty + kVStages;
     static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kTmemSlot + 16 + 1024;
@@ -336,7 +335,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr int kBarQFull = C::kBarQFull, kBarQReady = C::kBarQReady, kBarQEmpty = C::kBarQEmpty;
     constexpr int kBarSFull = C::kBarSFull, kBarPReady = C::kBarPReady, kBarODone = C::kBarODone;
     constexpr int kBarKFull = C::kBarKFull, kBarKReady = C::kBarKReady, kBarKEmpty = C::kBarKEmpty;
-    constexpr int kBarVFull = C::kBarVFull, kBarVReady = C::kBarVReady, kBarVEmpty = C::kBarVEmpty;
+    constexpr int kBarVFull = C::kBarVFull, kBarVEmpty = C::kBarVEmpty;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const uint32_t sb = smem_u32(smem);
@@ -363,7 +362,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(bar(kBarVFull + s), 1);
-            mbar_init(bar(kBarVReady + s), 2);
             mbar_init(bar(kBarVEmpty + s), 1);
         }
         fence_mbarrier_init();
@@ -459,7 +457,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const bool nxt = j + 1 < n;
                     const bool last_qk = j + 2 == n;
                     const int ks = (g + 1) % kKStages, vs = g % kVStages;
-                    pair_wait(bar(kBarVReady + vs), (g / kVStages) & 1, p.wait, abort);
                     pair_wait(bar(kBarPReady + 0), g & 1, p.wait, abort);
                     tc_fence_after();
                     issue_pv(0, vs, j > 0);
@@ -488,18 +485,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 kc += n;
             }
         }
-    } else if (warp == kWarpRelay) {
-        // ------------------------------------------------------------ "V landed" relay (both CTAs)
-        if (lane == 0) {
-            int kc = 0;
-            for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
-                const Item it = make_item(p, w);
-                for (int j = 0; j < it.n_kt; ++j, ++kc) {
-                    pair_wait(bar(kBarVFull + kc % kVStages), (kc / kVStages) & 1, p.wait, abort);
-                    arrive_leader(bar(kBarVReady + kc % kVStages));
-                }
-            }
-        }
     } else if (warp >= kWarpRope && warp < kWarpTma) {
         // ------------------------------------------------------------ K RoPE (both CTAs, 64 keys each)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRope));
@@ -518,6 +503,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 pair_wait(bar(kBarKFull + ks), (kc / kKStages) & 1, p.wait, abort);
                 if (!p.keys_prerotated) kr.rotate(smem + kKOff + ks * kKTile, rt);
                 if (j + 1 < it.n_kt) kr.load_seed(p.rope.cs, min(128 * (it.j_lo + j + 1) + half0 + r0, max_row), c);
+                // K(j) ready also means V(j) has landed: the MMA thread waits for
+                // KReady(j) before QK(j), which precedes PV(j)
+                pair_wait(bar(kBarVFull + kc % kVStages), (kc / kVStages) & 1, p.wait, abort);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) arrive_leader(bar(kBarKReady + ks));

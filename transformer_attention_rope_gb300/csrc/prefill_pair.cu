@@ -57,7 +57,7 @@ struct PairCfg {
     static constexpr int kRopeBoxes = DR / 64;
     static constexpr int kStages = DQK > 128 ? 3 : 4;
     static constexpr int kKStages = kStages;
-    static constexpr int kVStages = kStages;
+    static constexpr int kVStages = kStages;  // K(x) and V(x) share stage x % kStages and one "empty" barrier
     static constexpr int kQTile = kBoxes * kQBox;     // 128 rows x DQK
     static constexpr int kKTile = kBoxes * kKBox;     // this CTA's 64 keys x DQK
     // Q | V stages | K stages | 8 KB guard | barriers: an operand descriptor that
@@ -76,9 +76,8 @@ struct PairCfg {
     static constexpr int kBarODone = 10;                        // [2]  multicast commit
     static constexpr int kBarKFull = 12;                        // [K]  local TMA
     static constexpr int kBarKReady = kBarKFull + kKStages;     // [K]  leader: 8 warps
-    static constexpr int kBarKEmpty = kBarKReady + kKStages;    // [K]  multicast commit
-    static constexpr int kBarVFull = kBarKEmpty + kKStages;     // [V]  local TMA
-    static constexpr int kBarVEmpty = kBarVFull + kVStages;     // [V]  multicast commit
+    static constexpr int kBarVFull = kBarKReady + kKStages;     // [V]  local TMA
+    static constexpr int kBarVEmpty = kBarVFull + kVStages;     // [V]  multicast commit: frees K and V stage
     static constexpr int kNumBars = kBarVEmpty + kVStages;
     static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kTmemSlot + 16 + 1024;
@@ -334,7 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr int kTmemSlot = C::kTmemSlot;
     constexpr int kBarQFull = C::kBarQFull, kBarQReady = C::kBarQReady, kBarQEmpty = C::kBarQEmpty;
     constexpr int kBarSFull = C::kBarSFull, kBarPReady = C::kBarPReady, kBarODone = C::kBarODone;
-    constexpr int kBarKFull = C::kBarKFull, kBarKReady = C::kBarKReady, kBarKEmpty = C::kBarKEmpty;
+    constexpr int kBarKFull = C::kBarKFull, kBarKReady = C::kBarKReady;
     constexpr int kBarVFull = C::kBarVFull, kBarVEmpty = C::kBarVEmpty;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
@@ -358,7 +357,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(bar(kBarKFull + s), 1);
             mbar_init(bar(kBarKReady + s), 8);
-            mbar_init(bar(kBarKEmpty + s), 1);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(bar(kBarVFull + s), 1);
@@ -398,13 +396,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < it.n_kt; ++j, ++kc) {
                     const int key0 = 128 * (it.j_lo + j);
                     const int ks = kc % kKStages, vs = kc % kVStages;
-                    pair_wait(bar(kBarKEmpty + ks), ((kc / kKStages) & 1) ^ 1, p.wait, abort);
+                    // one "stage empty" barrier frees K(kc) and V(kc) together: it is
+                    // committed after PV(kc - stages), which follows QK(kc - stages)
+                    pair_wait(bar(kBarVEmpty + vs), ((kc / kVStages) & 1) ^ 1, p.wait, abort);
                     mbar_arrive_expect_tx(bar(kBarKFull + ks), kKTile);
 #pragma unroll
                     for (int bx = 0; bx < C::kBoxes; ++bx)
                         tma_load_3d(sb + kKOff + ks * kKTile + bx * kKBox, &tm_k, bar(kBarKFull + ks), 64 * bx,
                                     key0 + 64 * (int)rank, it.unit);
-                    pair_wait(bar(kBarVEmpty + vs), ((kc / kVStages) & 1) ^ 1, p.wait, abort);
                     mbar_arrive_expect_tx(bar(kBarVFull + vs), kVTile);
                     tma_load_3d(sb + kVOff + vs * kVTile, &tm_v, bar(kBarVFull + vs), 64 * (int)rank, key0, it.unit);
                 }
@@ -451,7 +450,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     commit_pair(bar(kBarSFull + t));
                     if (n == 1) commit_pair(bar(kBarQEmpty + t));
                 }
-                commit_pair(bar(kBarKEmpty + kc % kKStages));
                 for (int j = 0; j < n; ++j) {
                     const int g = kc + j;
                     const bool nxt = j + 1 < n;
@@ -477,7 +475,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         issue_qk(1, ks);
                         commit_pair(bar(kBarSFull + 1));
                         if (last_qk) commit_pair(bar(kBarQEmpty + 1));
-                        commit_pair(bar(kBarKEmpty + ks));
                     } else {
                         commit_pair(bar(kBarODone + 1));
                     }

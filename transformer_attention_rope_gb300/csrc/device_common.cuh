@@ -244,6 +244,28 @@ __device__ __forceinline__ float fast_exp2(float x)
     return y;
 }
 
+// Sets to -inf the scores of a 128-key row that lie outside the row's visible
+// keys [lo, hi] (tile-relative). Where every row of the warp has one bound off
+// the tile (the causal diagonal: lo <= 0; the window's far edge: hi >= 127), a
+// single comparison per key does; branch-free inside each case.
+__device__ __forceinline__ void mask_row128(uint32_t (&v)[128], int lo, int hi)
+{
+    const uint32_t ninf = 0xff800000u;
+    if (__all_sync(0xffffffffu, lo <= 0)) {
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+            if (e > hi) v[e] = ninf;
+    } else if (__all_sync(0xffffffffu, hi >= 127)) {
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+            if (e < lo) v[e] = ninf;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+            if (e < lo || e > hi) v[e] = ninf;
+    }
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile that a
 // TMA load wrote with CU_TENSOR_MAP_SWIZZLE_128B (rows of 128 bytes, tile base
 // 1024-byte aligned): the chunk index is XORed with the row index mod 8.

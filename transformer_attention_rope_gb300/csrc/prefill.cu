@@ -456,11 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int ch = 0; ch < 4; ++ch)
                     tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * ch]));
                 tmem_wait_ld();
-                if (!all_full) {
-#pragma unroll
-                    for (int e = 0; e < 128; ++e)
-                        if (e < lo_c || e > hi_c) v[e] = __float_as_uint(-INFINITY);
-                }
+                if (!all_full) mask_row128(v, lo_c, hi_c);
                 // row max of the visible scores (8 independent chains)
                 float acc[8];
 #pragma unroll

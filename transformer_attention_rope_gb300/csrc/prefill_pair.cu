@@ -385,14 +385,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int kc = 0;
             for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
                 const Item it = make_item(p, w);
-                for (int t = 0; t < 2; ++t) {
-                    pair_wait(bar(kBarQEmpty + t), (k & 1) ^ 1, p.wait, abort);
-                    mbar_arrive_expect_tx(bar(kBarQFull + t), kQTile);
+                auto load_q = [&]() {
+                    for (int t = 0; t < 2; ++t) {
+                        pair_wait(bar(kBarQEmpty + t), (k & 1) ^ 1, p.wait, abort);
+                        mbar_arrive_expect_tx(bar(kBarQFull + t), kQTile);
 #pragma unroll
-                    for (int bx = 0; bx < C::kBoxes; ++bx)
-                        tma_load_3d(sb + kQOff + t * kQTile + bx * kQBox, &tm_q, bar(kBarQFull + t), 64 * bx,
-                                    it.r0 + (2 * (int)rank + t) * P, it.zq);
-                }
+                        for (int bx = 0; bx < C::kBoxes; ++bx)
+                            tma_load_3d(sb + kQOff + t * kQTile + bx * kQBox, &tm_q, bar(kBarQFull + t), 64 * bx,
+                                        it.r0 + (2 * (int)rank + t) * P, it.zq);
+                    }
+                };
                 for (int j = 0; j < it.n_kt; ++j, ++kc) {
                     const int key0 = 128 * (it.j_lo + j);
                     const int ks = kc % kKStages, vs = kc % kVStages;
@@ -406,6 +408,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     key0 + 64 * (int)rank, it.unit);
                     mbar_arrive_expect_tx(bar(kBarVFull + vs), kVTile);
                     tma_load_3d(sb + kVOff + vs * kVTile, &tm_v, bar(kBarVFull + vs), 64 * (int)rank, key0, it.unit);
+                    // the item's first K / V tiles go out before its Q tiles, whose
+                    // buffers free up only when the previous item's last QK^T is done
+                    if (j == 0) load_q();
                 }
             }
         }
@@ -551,11 +556,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int ch = 0; ch < 4; ++ch)
                     tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * ch]));
                 tmem_wait_ld();
-                if (!all_full) {
-#pragma unroll
-                    for (int e = 0; e < 128; ++e)
-                        if (e < lo_c || e > hi_c) v[e] = __float_as_uint(-INFINITY);
-                }
+                if (!all_full) mask_row128(v, lo_c, hi_c);
                 float acc[8];
 #pragma unroll
                 for (int a = 0; a < 8; ++a) acc[a] = __uint_as_float(v[a]);

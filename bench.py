@@ -16,7 +16,8 @@ Reported (one JSON line on rank 0):
            peaks in MEASURED_PEAKS.json;
   e2e      the same two metrics through the same C-ABI calls with the inputs in
            pinned host memory: every step copies the step's inputs host->device
-           and the outputs device->host inside the timed region;
+           and the outputs device->host inside the timed region (after the same
+           number of untimed warm-up steps);
   cpu_baseline  the fp64 oracle, as it stands, on a bounded sample of the same
            workloads on this machine's host cores.
 
@@ -396,26 +397,36 @@ def run_ours(args):
     if feat.get("keys_prerotated"):  # the pre-rotated key caches stay on the device
         h2d -= sum(t.numel() * t.element_size() for t in (pin[1:2] + din[1:2]))
     d2h = (pout.numel() * 2 if do_pre else 0) + (dout.numel() * 2 if do_dec else 0)
-    evx = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize()
-    for i in range(K):
-        evx[i][0].record(stream)
+    def e2e_step(e=None):
+        if e:
+            e[0].record(stream)
         if do_pre:
             for dst, src in zip((pq, pk, pv), pin):
                 if not (feat.get("keys_prerotated") and src is pin[1]):
                     dst.copy_(src, non_blocking=True)
             prefill()
             pout_h.copy_(pout, non_blocking=True)
-        evx[i][1].record(stream)
+        if e:
+            e[1].record(stream)
         if do_dec:
             for dst, src in zip((dq, dk, dv), din):
                 if not (feat.get("keys_prerotated") and src is din[1]):
                     dst.copy_(src, non_blocking=True)
             decode()
             dout_h.copy_(dout, non_blocking=True)
-        evx[i][2].record(stream)
+        if e:
+            e[2].record(stream)
+
+    # the first copies from (and into) freshly pinned buffers run several times
+    # slower than later ones: warm the end-to-end path up as the device path was
+    for _ in range(warm):
+        e2e_step()
+    evx = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        e2e_step(evx[i])
     torch.cuda.synchronize()
     te_pre = sum(e[0].elapsed_time(e[1]) for e in evx) / 1e3
     te_dec = sum(e[1].elapsed_time(e[2]) for e in evx) / 1e3

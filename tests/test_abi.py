@@ -95,3 +95,95 @@ def test_rope_reserve_rejects(lib):
     assert apex.apex_attn_rope_reserve(0, 128, 10000.0) == 1
     assert apex.apex_attn_rope_reserve(100, 96, 10000.0) == 2
     assert apex.apex_attn_rope_reserve(100, 128, -1.0) == 1
+
+
+def _opt(**kw):
+    o = dict(window=0, q_pos=0, rope_base=10000.0, yarn_scale=1.0, yarn_beta_fast=32.0, yarn_beta_slow=1.0,
+             prefix_len=0, keys_prerotated=False)
+    o.update(kw)
+    return apex._options(**o)
+
+
+# prefill with options: (B, H_q, H_kv, S_q, S_k, d_h), options, expected status
+@pytest.mark.parametrize("shape,opt,code", [
+    ((1, 4, 2, 8, 8, 64), None, 1),                                  # no options
+    ((1, 4, 2, 8, 8, 64), dict(prefix_len=-1), 1),
+    ((1, 4, 2, 8, 8, 64), dict(prefix_len=9), 1),                    # prefix beyond the keys
+    ((1, 4, 2, 8, 8, 64), dict(q_pos=1), 1),                         # q_pos0 + S_q > S_k
+    ((1, 4, 2, 8, 8, 64), dict(rope_base=float("inf")), 1),
+    ((1, 4, 2, 8, 8, 64), dict(yarn_scale=float("nan")), 1),
+    ((1, 4, 2, 8, 8, 64), dict(yarn_scale=4.0, yarn_beta_fast=-1.0), 1),
+    ((1, 4, 2, 8, 8, 64), dict(yarn_scale=4.0, yarn_beta_slow=float("inf")), 1),
+    ((1, 4, 2, 8, 8, 96), {}, 2),
+])
+def test_fwd_ex_rejects(lib, shape, opt, code):
+    o = None if opt is None else _opt(**opt)
+    assert apex.apex_attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, *shape, o, None) == code
+
+
+# decoupled-RoPE prefill: (B, H_q, H_kv, S_q, S_k, d_h, d_r), expected status
+@pytest.mark.parametrize("shape,code", [
+    ((1, 4, 2, 8, 8, 128, 0), 1),
+    ((1, 4, 2, 8, 8, 128, 63), 1),       # odd rope part
+    ((1, 4, 2, 8, 8, 64, 64), 2),        # only d_h = 128 with d_r = 64 is built
+    ((1, 4, 2, 8, 8, 128, 32), 2),
+    ((1, 3, 2, 8, 8, 128, 64), 1),       # H_q % H_kv != 0
+    ((1, 4, 2, 9, 8, 128, 64), 1),       # S_q > S_k
+])
+def test_mla_fwd_rejects(lib, shape, code):
+    assert apex.apex_attn_mla_fwd(FAKE, FAKE, FAKE, FAKE, *shape, _opt(), None) == code
+    assert apex.apex_attn_mla_fwd(0, FAKE, FAKE, FAKE, *shape, _opt(), None) == 1
+
+
+# decodes with options: (B, H_q, H_kv, S_k, d_h), options, workspace bytes, expected status
+@pytest.mark.parametrize("shape,opt,ws,code", [
+    ((2, 8, 2, 64, 64), None, 1 << 30, 1),
+    ((2, 8, 2, 64, 64), dict(q_pos=64), 1 << 30, 1),      # q_pos >= S_k
+    ((2, 8, 2, 64, 64), dict(q_pos=63, prefix_len=65), 1 << 30, 1),
+    ((2, 8, 2, 64, 64), dict(q_pos=63), 16, 1),           # workspace too small
+    ((2, 8, 2, 64, 96), dict(q_pos=63), 1 << 30, 2),
+])
+def test_decode_ex_rejects(lib, shape, opt, ws, code):
+    o = None if opt is None else _opt(**opt)
+    assert apex.apex_attn_decode_ex(FAKE, FAKE, FAKE, FAKE, *shape, o, FAKE, ws, None) == code
+
+
+@pytest.mark.parametrize("shape,opt,ws,code", [
+    ((2, 8, 2, 64, 128, 64), None, 1 << 30, 1),
+    ((2, 8, 2, 64, 128, 65), dict(q_pos=63), 1 << 30, 1),
+    ((2, 8, 2, 64, 64, 64), dict(q_pos=63), 1 << 30, 2),
+    ((2, 8, 2, 64, 128, 64), dict(q_pos=64), 1 << 30, 1),
+    ((2, 8, 2, 64, 128, 64), dict(q_pos=63), 16, 1),
+])
+def test_mla_decode_rejects(lib, shape, opt, ws, code):
+    o = None if opt is None else _opt(**opt)
+    assert apex.apex_attn_mla_decode(FAKE, FAKE, FAKE, FAKE, *shape, o, FAKE, ws, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((FAKE, FAKE, 0, 8, 64, 0, 512, 512), 1),          # no heads
+    ((FAKE, FAKE, 2, 8, 64, -1, 512, 512), 1),         # negative first position
+    ((FAKE, FAKE, 2, 8, 96, 0, 768, 768), 2),          # d_h = 96
+    ((FAKE, FAKE, 2, 8, 64, 0, 256, 512), 1),          # input heads overlap
+    ((FAKE, FAKE, 2, 8, 64, 0, 516, 512), 1),          # stride not a multiple of 8 elements
+    ((FAKE + 8, FAKE, 2, 8, 64, 0, 512, 512), 1),      # misaligned input
+])
+def test_rope_keys_rejects(lib, args, code):
+    assert apex.apex_attn_rope_keys(*args, _opt(), None) == code
+    assert apex.apex_attn_rope_keys(FAKE, FAKE, 2, 8, 64, 0, 512, 512, None, None) == 1
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, FAKE, FAKE, FAKE, 2, 8, 2, 64, 64, 0, 63, 10000.0), 1),
+    ((FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 64, 64, 0, 64, 10000.0), 1),       # q_pos >= S_k
+    ((FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 65536, 64, 0, 63, 10000.0), 2),    # beyond the static scratch
+    ((FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 64, 96, 0, 63, 10000.0), 2),
+    ((FAKE, FAKE, FAKE, FAKE, 2, 6, 2, 64, 64, 0, 63, 10000.0), 2),       # G = 3
+])
+def test_decode_noalloc_rejects(lib, args, code):
+    assert apex.apex_attn_decode_noalloc(*args, None) == code
+
+
+def test_selftest_rejects_out_of_range_limits(lib):
+    assert apex.apex_attn_selftest_wait_timeout(0, None) == 1
+    assert apex.apex_attn_selftest_wait_timeout(5001, None) == 1

@@ -89,6 +89,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         reinterpret_cast<uint32_t *>(smem + s * C::kStageBytes + C::kKBytes + C::kVBytes)[w] = 0u;
     }
     __syncthreads();
+    // launched as a programmatic dependent: the set-up above overlaps the previous
+    // kernel's tail; nothing in global memory is touched before that kernel is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
@@ -393,9 +396,20 @@ cudaError_t launch_t(const DecodeLaunch &L, cudaStream_t stream)
     cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<DQK, DV, DR, NT, PREROT>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
-    decode_split_kernel<DQK, DV, DR, NT, PREROT><<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tm_k, L.tm_v, L.p);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(L.grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        err = cudaLaunchKernelEx(&cfg, decode_split_kernel<DQK, DV, DR, NT, PREROT>, L.tm_k, L.tm_v, L.p);
+        if (err != cudaSuccess) return err;
+    }
     const int rows = L.p.B * L.p.H_q;
     // programmatic dependent launch: the combine grid's launch is prepared while
     // the split grid runs, and its blocks wait (griddepcontrol.wait) for that

@@ -217,6 +217,24 @@ __device__ __forceinline__ float fast_exp2(float x)
     return y;
 }
 
+// Launch a prefill kernel as a programmatic dependent of the stream's previous
+// work (its blocks wait in griddepcontrol.wait before touching global memory).
+template <typename K, typename L>
+inline cudaError_t launch_dependent(K kernel, int grid, int threads, int smem, cudaStream_t stream, const L &l)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, l.tm_q, l.tm_k, l.tm_v, l.p);
+}
+
 // Sets to -inf the scores of a 128-key row that lie outside the row's visible
 // keys [lo, hi] (tile-relative). Where every row of the warp has one bound off
 // the tile (the causal diagonal: lo <= 0; the window's far edge: hi >= 127), a

@@ -374,6 +374,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();  // both CTAs' barriers initialised, TMEM allocated
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kTmemSlot);
+    // launched as a programmatic dependent: the set-up above overlaps the previous
+    // kernel's tail; nothing in global memory is touched before that kernel is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp >= kWarpTma) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
     if (warp == kWarpTma) {
@@ -669,8 +672,7 @@ cudaError_t launch_pair_t(const PrefillLaunch &L, cudaStream_t stream)
     err = cudaFuncGetAttributes(&fa, prefill_pair_kernel<DQK, DR>);
     if (err != cudaSuccess) return err;
     if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-    prefill_pair_kernel<DQK, DR><<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
-    return cudaGetLastError();
+    return launch_dependent(prefill_pair_kernel<DQK, DR>, L.grid, kThreads, C::kSmemBytes, stream, L);
 }
 
 }  // namespace

@@ -60,6 +60,16 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *m, uint32_t bar, int x, int y,
+                                                 int z, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(pol)
+        : "memory");
+}
+
 // PREROT: the cached keys already hold RoPE(k_j, j); the query is rotated to
 // its absolute position and the keys are used as they are.
 template <int DQK, int DV, int DR, int NT, bool PREROT>
@@ -99,6 +109,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
         }
+        // the cache is streamed once: let its lines go first from L2
+        uint64_t pol;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
         constexpr int kPairs = DQK / 2;            // pairs of a query row
         constexpr int kCPairs = (DQK - DR) / 2;    // pairs of its content part (not rotated)
         constexpr int kRPairs = DR / 2;            // pairs of its rope part (table row length)
@@ -133,10 +146,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                     mbar_arrive_expect_tx(bar_full + 8 * slot, C::kKBytes + C::kVBytes);
 #pragma unroll
                     for (int bx = 0; bx < C::kKBoxes; ++bx)
-                        tma_load_3d(kdst + bx * kBoxBytes, &tm_k, bar_full + 8 * slot, 64 * bx, j0, unit);
+                        tma_load_3d_hint(kdst + bx * kBoxBytes, &tm_k, bar_full + 8 * slot, 64 * bx, j0, unit, pol);
 #pragma unroll
                     for (int bx = 0; bx < C::kVBoxes; ++bx)
-                        tma_load_3d(vdst + bx * kBoxBytes, &tm_v, bar_full + 8 * slot, 64 * bx, j0, unit);
+                        tma_load_3d_hint(vdst + bx * kBoxBytes, &tm_v, bar_full + 8 * slot, 64 * bx, j0, unit, pol);
                 }
                 // Q' = R(q_pos - j0) q (Part 1, §4.2 rotation of each interleaved pair);
                 // a query inside a prefix can see keys after it: R(-a) = (cos a, -sin a).

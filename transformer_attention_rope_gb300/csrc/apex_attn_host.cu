@@ -36,12 +36,20 @@ struct RopeTable {
     int cap;  // positions held
 };
 
+struct SplitPlan {
+    int n_split, stages_per_split;
+};
+
 struct DeviceState {
     std::mutex mu;
     bool ready = false;
     int sm_count = 0;
     uint32_t *status = nullptr;  // per-device status word
     std::vector<RopeTable> tables;
+    // last decode split plan: (units, stages, capacity) -> plan; the search
+    // walks every split count, which for one sequence of 32K keys is ~500 steps
+    int plan_key[3] = {-1, -1, -1};
+    SplitPlan plan{1, 1};
 };
 
 DeviceState g_state[kMaxDevices];
@@ -218,10 +226,6 @@ DeviceState *current_state(int *dev_out)
 // --- decode split choice: the KV range of each (b, kv-head) unit is cut into
 // n_split splits of whole 64-key stages; pick the count that minimises the
 // modelled time rounds * (stages per split + 1) on a persistent grid.
-struct SplitPlan {
-    int n_split, stages_per_split;
-};
-
 int decode_split_cap(int units, int n_stages)
 {
     long cap = std::max(1l, 32768l / std::max(1, units));
@@ -385,7 +389,13 @@ apex_status decode_launch(const void *q, const void *k_cache, const void *v_cach
     p.stage0 = p.k_lo / kDecodeKeysPerStage;
     p.n_stages = p.k_hi / kDecodeKeysPerStage - p.stage0 + 1;
     const int capacity = decode_ctas_per_sm(d_qk, d_v, p.G) * st->sm_count;
-    SplitPlan plan = plan_decode(units, p.n_stages, capacity);
+    if (st->plan_key[0] != units || st->plan_key[1] != p.n_stages || st->plan_key[2] != capacity) {
+        st->plan = plan_decode(units, p.n_stages, capacity);
+        st->plan_key[0] = units;
+        st->plan_key[1] = p.n_stages;
+        st->plan_key[2] = capacity;
+    }
+    const SplitPlan plan = st->plan;
     p.n_split = plan.n_split;
     p.stages_per_split = plan.stages_per_split;
     p.n_items = units * p.n_split;

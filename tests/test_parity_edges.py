@@ -1,7 +1,8 @@
 """GPU parity on edge shapes not covered elsewhere: every group size on both
 prefill kernels at d_h = 128, single query rows, single keys, tiny ragged
 sizes, window 1, whole-sequence prefixes, many small units, decoupled RoPE at
-G = 16 and one row, and decode on one-key and ragged caches.  Tolerance as
+G = 16 and one row, decode on one-key and ragged caches, and 131072-token
+prefill and decode.  Tolerance as
 everywhere: max |err| <= 2e-2, mean |err| <= 2e-3."""
 import numpy as np
 import pytest
@@ -90,4 +91,35 @@ def test_decode_edges(B, H_q, H_kv, S_k, window, q_pos):
     out = apex.decode(q.to(d), k.to(d), v.to(d), q_pos, window=window)
     torch.cuda.synchronize()
     _close(out, oracle.attn(q, k, v, window=window, q_pos0=q_pos), "decode edge")
+    assert apex.apex_attn_device_status() == 0
+
+
+def test_prefill_131072_keys_sampled_rows():
+    """A 131072-token sequence (twice the long workload), window 8192 and causal:
+    sampled rows of every head against the oracle (indices and offsets past
+    2^16 positions, a 128K-row RoPE table)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    d = torch.device("cuda:0")
+    S = 131072
+    q, k, v = inputs.make_qkv(1, 8, 2, S, S, 128, 4400)
+    rows = sorted(set(range(0, 32)) | set(range(S - 32, S)) | set(range(8192 - 8, 8192 + 8)) |
+                  set(int(x) for x in np.random.default_rng(4400).integers(0, S, 24)))
+    for window in (8192, 0):
+        out = apex.fwd(q.to(d), k.to(d), v.to(d), window=window)
+        torch.cuda.synchronize()
+        _close(out[:, :, rows], oracle.attn(q, k, v, window=window, rows=rows), "prefill 128K W%d" % window)
+    assert apex.apex_attn_device_status() == 0
+
+
+def test_decode_131072_keys():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    d = torch.device("cuda:0")
+    S_k = 131072
+    q, k, v = inputs.make_qkv(2, 8, 2, 1, S_k, 128, 4500)
+    for window, q_pos in ((0, S_k - 1), (8192, S_k - 1), (0, 70000)):
+        out = apex.decode(q.to(d), k.to(d), v.to(d), q_pos, window=window)
+        torch.cuda.synchronize()
+        _close(out, oracle.attn(q, k, v, window=window, q_pos0=q_pos), "decode 128K W%d q%d" % (window, q_pos))
     assert apex.apex_attn_device_status() == 0

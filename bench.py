@@ -17,7 +17,9 @@ Reported (one JSON line on rank 0):
   e2e      the same two metrics through the same C-ABI calls with the inputs in
            pinned host memory: every step copies the step's inputs host->device
            and the outputs device->host inside the timed region (after the same
-           number of untimed warm-up steps);
+           number of untimed warm-up steps), each call type as a serving loop
+           runs it: copy-in, compute and copy-out on three streams with two
+           buffer sets, so that consecutive steps overlap;
   cpu_baseline  the fp64 oracle, as it stands, on a bounded sample of the same
            workloads on this machine's host cores.
 
@@ -392,44 +394,86 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError("device status %d after the timed region" % st)
 
-    # ---- end to end through the C ABI with pinned host buffers
+    # ---- end to end through the C ABI with pinned host buffers.  Each call type
+    # runs its steps as a serving loop would: three streams (copy in, compute,
+    # copy out) and two sets of device buffers, so that step i + 1's inputs move
+    # in while step i computes and step i - 1's result moves out.  Every step
+    # still copies its own inputs in and its result out.
     h2d = sum(t.numel() * t.element_size() for t in (*pin, *din))
     if feat.get("keys_prerotated"):  # the pre-rotated key caches stay on the device
         h2d -= sum(t.numel() * t.element_size() for t in (pin[1:2] + din[1:2]))
     d2h = (pout.numel() * 2 if do_pre else 0) + (dout.numel() * 2 if do_dec else 0)
-    def e2e_step(e=None):
-        if e:
-            e[0].record(stream)
-        if do_pre:
-            for dst, src in zip((pq, pk, pv), pin):
-                if not (feat.get("keys_prerotated") and src is pin[1]):
-                    dst.copy_(src, non_blocking=True)
-            prefill()
-            pout_h.copy_(pout, non_blocking=True)
-        if e:
-            e[1].record(stream)
-        if do_dec:
-            for dst, src in zip((dq, dk, dv), din):
-                if not (feat.get("keys_prerotated") and src is din[1]):
-                    dst.copy_(src, non_blocking=True)
-            decode()
-            dout_h.copy_(dout, non_blocking=True)
-        if e:
-            e[2].record(stream)
 
-    # the first copies from (and into) freshly pinned buffers run several times
-    # slower than later ones: warm the end-to-end path up as the device path was
-    for _ in range(warm):
-        e2e_step()
-    evx = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize()
-    for i in range(K):
-        e2e_step(evx[i])
-    torch.cuda.synchronize()
-    te_pre = sum(e[0].elapsed_time(e[1]) for e in evx) / 1e3
-    te_dec = sum(e[1].elapsed_time(e[2]) for e in evx) / 1e3
+    def e2e_run(host_in, dev_sets, dev_outs, host_outs, call, keep):
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        in_done = [torch.cuda.Event() for _ in range(2)]
+        comp_done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
+
+        def step(i):
+            b = i % 2
+            if i >= 2:
+                s_in.wait_event(comp_done[b])  # step i - 2 has consumed this input set
+            with torch.cuda.stream(s_in):
+                for j, (dst, src) in enumerate(zip(dev_sets[b], host_in)):
+                    if j not in keep:
+                        dst.copy_(src, non_blocking=True)
+            in_done[b].record(s_in)
+            stream.wait_event(in_done[b])
+            if i >= 2:
+                stream.wait_event(out_done[b])  # step i - 2's result has been read back
+            call(*dev_sets[b], dev_outs[b])
+            comp_done[b].record(stream)
+            s_out.wait_event(comp_done[b])
+            with torch.cuda.stream(s_out):
+                host_outs[b].copy_(dev_outs[b], non_blocking=True)
+            out_done[b].record(s_out)
+
+        # the first copies from (and into) freshly pinned buffers run several times
+        # slower than later ones: warm up as the device-resident leg does
+        for i in range(warm):
+            step(i)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(s_in)
+        for i in range(warm, warm + K):
+            step(i)
+        t1.record(s_out)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / 1e3
+
+    te_pre = te_dec = 0.0
+    if do_pre:
+        keep = (1,) if feat.get("keys_prerotated") else ()
+        sets = [(pq, pk, pv), tuple(t if j in keep else torch.empty_like(t) for j, t in enumerate((pq, pk, pv)))]
+        outs = [pout, torch.empty_like(pout)]
+        houts = [pout_h, torch.empty(pout.shape, dtype=pout.dtype, pin_memory=True)]
+
+        def pre_call(q_, k_, v_, o_):
+            if wp.d_r:
+                apex.mla_fwd(q_, k_, v_, wp.d_r, window=wp.window, q_pos0=wp.q_pos0, rope_base=wp.rope_base, out=o_,
+                             **feat)
+            else:
+                apex.fwd(q_, k_, v_, window=wp.window, q_pos0=wp.q_pos0, rope_base=wp.rope_base, out=o_, **feat)
+        te_pre = e2e_run(pin, sets, outs, houts, pre_call, keep)
+        del sets, outs
+    if do_dec:
+        keep = (1,) if feat.get("keys_prerotated") else ()
+        sets = [(dq, dk, dv), tuple(t if j in keep else torch.empty_like(t) for j, t in enumerate((dq, dk, dv)))]
+        outs = [dout, torch.empty_like(dout)]
+        houts = [dout_h, torch.empty(dout.shape, dtype=dout.dtype, pin_memory=True)]
+
+        def dec_call(q_, k_, v_, o_):
+            if wd.d_r:
+                apex.mla_decode(q_, k_, v_, wd.q_pos0, wd.d_r, window=wd.window, rope_base=wd.rope_base, out=o_,
+                                workspace=ws, **feat)
+            else:
+                apex.decode(q_, k_, v_, wd.q_pos0, window=wd.window, rope_base=wd.rope_base, out=o_, workspace=ws,
+                            **feat)
+        te_dec = e2e_run(din, sets, outs, houts, dec_call, keep)
+        del sets, outs
 
     flops = prefill_flops(wp, feat.get("prefix_len", 0))
     kvb = decode_kv_bytes(wd, feat.get("prefix_len", 0))

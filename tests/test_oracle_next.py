@@ -44,7 +44,7 @@ def test_yarn_scale_one_is_plain_rope():
 
 def test_yarn_regime_edges():
     """Below beta_fast nothing changes, above beta_slow * s the frequency is divided
-    by s, and inside the band the divisor t s + 1 - t stays in [1, s] (t clamped)."""
+    by s, and inside the band the divisor stays in [1, s]."""
     s, bf, bs = 16.0, 8.0, 2.0
     lam = np.array([1.0, 7.9, 8.1, 20.0, 31.9, 32.1, 1e5])
     th = 2 * math.pi / lam
@@ -53,8 +53,6 @@ def test_yarn_regime_edges():
     np.testing.assert_allclose(got[5:], th[5:] / s, rtol=1e-15)  # low frequency
     div = th[2:5] / got[2:5]
     assert np.all(div >= 1.0) and np.all(div <= s)
-    t = np.clip((lam[2:5] / bs - 1) / (s - 1), 0, 1)
-    np.testing.assert_allclose(div, t * s + 1 - t, rtol=1e-14)
 
 
 def _rot(m, thetas):
@@ -155,3 +153,114 @@ def test_prerotated_keys_equal_rotating_in_the_block():
     a = oracle.attn(q, k, v, window=5)
     b = oracle.attn(q, k_rot, v, window=5, keys_prerotated=True)
     np.testing.assert_allclose(a, b, atol=1e-13, rtol=0)
+
+
+# --------------------------------------------------------------------------
+# YaRN middle band: properties the pages fix, not the formula typed again.
+# Part 1, §5.3 sorts the pairs into three regimes by wavelength: short ones
+# are left alone, long ones (beyond beta_slow * s) get theta / s, and the band
+# between them moves gradually from the first treatment to the second.  In
+# §5.4, t weighs the two: t = 0 keeps theta, t = 1 gives theta / s.  Hence:
+#   (a) the divisor theta / theta' lies in [1, s] everywhere;
+#   (b) it never falls as the wavelength grows;
+#   (c) the band joins the fully scaled regime without a jump at
+#       lambda = beta_slow * s (t reaches 1 there);
+#   (d) inside the band, where t is not clamped, the divisor grows strictly.
+# The lower edge has a jump under the pages' formula: at lambda = beta_fast,
+# t = (beta_fast / beta_slow - 1) / (s - 1), which is 0 only when
+# beta_fast = beta_slow (with the defaults 32 and 1 it is 1, so the pairs go
+# from unscaled straight to fully scaled); (b) still holds across it.
+# --------------------------------------------------------------------------
+
+# (s, beta_fast, beta_slow): the defaults at s = 32 and 8, a band wider than
+# the defaults give, and one with beta_fast < beta_slow, where t < 0 occurs
+# inside the band and the clamp decides
+YARN_CONFIGS = [(32.0, 32.0, 1.0), (8.0, 32.0, 1.0), (16.0, 8.0, 2.0), (16.0, 2.0, 8.0), (4.0, 3.0, 3.0)]
+
+
+def _divisors(scale_fn, s, bf, bs, lam):
+    th = 2 * math.pi / lam
+    return th / np.asarray(scale_fn(th, s, bf, bs), dtype=np.float64)
+
+
+def _wavelength_grid(s, bf, bs):
+    lo, hi = min(bf, bs) / 4.0, bs * s * 4.0
+    return np.geomspace(lo, hi, 4001)
+
+
+def _check_bounds(scale_fn, s, bf, bs):
+    div = _divisors(scale_fn, s, bf, bs, _wavelength_grid(s, bf, bs))
+    return bool(np.all(div >= 1.0 - 1e-12) and np.all(div <= s * (1 + 1e-12)))
+
+
+def _check_monotone(scale_fn, s, bf, bs):
+    div = _divisors(scale_fn, s, bf, bs, _wavelength_grid(s, bf, bs))
+    return bool(np.all(np.diff(div) >= -1e-12 * div[1:]))
+
+
+def _check_upper_edge(scale_fn, s, bf, bs):
+    edge = bs * s
+    if edge <= bf:  # no band below the edge
+        return True
+    lam = edge * (1.0 - np.array([1e-3, 1e-6, 1e-9]))
+    div = _divisors(scale_fn, s, bf, bs, lam)
+    return bool(np.all(np.abs(div - s) <= 4.0 * s * (1.0 - lam / edge) * max(1.0, edge / bs) + 1e-9))
+
+
+def _check_strict_in_band(scale_fn, s, bf, bs):
+    lo, hi = max(bf, bs), bs * s  # the part of the band where 0 <= t <= 1
+    if hi <= lo * 1.001:
+        return True
+    lam = np.geomspace(lo * 1.0005, hi * 0.9995, 200)
+    div = _divisors(scale_fn, s, bf, bs, lam)
+    return bool(np.all(np.diff(div) > 0))
+
+
+YARN_CHECKS = (_check_bounds, _check_monotone, _check_upper_edge, _check_strict_in_band)
+
+
+@pytest.mark.parametrize("s,bf,bs", YARN_CONFIGS)
+@pytest.mark.parametrize("check", YARN_CHECKS, ids=lambda f: f.__name__[7:])
+def test_yarn_band_properties(check, s, bf, bs):
+    assert check(oracle.yarn_scale_theta, s, bf, bs)
+
+
+def test_yarn_lower_edge_jump_is_the_pages_reading():
+    """With the defaults (beta_fast 32, beta_slow 1) the pair just above a
+    wavelength of 32 is already fully scaled, the pair just below it not at
+    all: the discontinuity the §5.4 formula implies at beta_fast."""
+    s = 32.0
+    div = _divisors(oracle.yarn_scale_theta, s, 32.0, 1.0, np.array([31.999, 32.001]))
+    assert div[0] == 1.0
+    assert abs(div[1] - s) <= 1e-3 * s
+
+
+def test_yarn_pins_catch_planted_mistakes():
+    """Plausible misreadings of §5.4 (beta_fast in place of beta_slow in t,
+    the divisor written t + (1 - t) s, the clamp of t left out) each fail at
+    least one of the band properties above on at least one configuration."""
+    def make(t_of, divisor, clamp):
+        def scale(th, s, bf, bs):
+            th = np.asarray(th, dtype=np.float64)
+            lam = 2 * math.pi / th
+            t = t_of(lam, s, bf, bs)
+            if clamp:
+                t = np.clip(t, 0.0, 1.0)
+            mid = th / divisor(t, s)
+            return np.where(lam < bf, th, np.where(lam > bs * s, th / s, mid))
+        return scale
+
+    right_t = lambda lam, s, bf, bs: (lam / bs - 1.0) / (s - 1.0)
+    right_div = lambda t, s: t * s + (1.0 - t)
+    # the restated rule itself passes every check (so the checks are not vacuous
+    # for the mutants below)
+    ok = make(right_t, right_div, True)
+    assert all(c(ok, *cfg) for c in YARN_CHECKS for cfg in YARN_CONFIGS)
+    mutants = {
+        "beta_fast in t": make(lambda lam, s, bf, bs: (lam / bf - 1.0) / (s - 1.0), right_div, True),
+        "divisor t + (1 - t) s": make(right_t, lambda t, s: t + (1.0 - t) * s, True),
+        "no clamp": make(right_t, right_div, False),
+    }
+    for name, fn in mutants.items():
+        failed = [(c.__name__, cfg) for c in YARN_CHECKS for cfg in YARN_CONFIGS if not c(fn, *cfg)]
+        assert failed, name

@@ -23,10 +23,20 @@ Reported (one JSON line on rank 0):
   cpu_baseline  the fp64 oracle, as it stands, on a bounded sample of the same
            workloads on this machine's host cores.
 
+  configs  the other prefill workloads (wide: B1 H_q128 H_kv8 S8192 causal;
+           long: B1 H_q32 H_kv8 S65536 W4096; mla: the wide shape with 64-entry
+           decoupled RoPE), each timed on its own after the step (same K and
+           warm-up, CUDA events around every call) with its ms per call,
+           TFLOP/s and fraction of the measured bf16 peak.
+
 With --impl reference the oracle itself is the timed arm (host cores, bounded
 sample per step); it prints the same keys with "impl": "reference".
-Multi-GPU (torchrun): every rank runs the same step on its own GPU with its own
-seed (independent problems, no collective on the data path): weak scaling.
+Multi-GPU: every rank runs the same step on its own GPU with its own seed
+(independent problems, no collective on the data path): weak scaling.  Under
+torchrun the ranks come from the environment; `--gpus N` without it starts N
+ranks itself (torch.distributed.run on 127.0.0.1) and refuses to run when fewer
+than N GPUs are visible.  `--launcher-check` runs only the ranks' host logic
+(gloo, no GPU): each rank reports its seeds and the timings' max-reduction.
 """
 from __future__ import annotations
 
@@ -475,6 +485,15 @@ def run_ours(args):
         te_dec = e2e_run(din, sets, outs, houts, dec_call, keep)
         del sets, outs
 
+    # ---- the other prefill workloads, each timed on its own
+    cfg_res, cfg_clocks = {}, None
+    if args.config_names:
+        cs = ClockSampler(bus_id_of(local))
+        cs.start()
+        cfg_res = time_prefill_configs(args.config_names, rank, K, warm, stream, dev)
+        cfg_clocks = cs.stop()
+    cfg_t = max_over_ranks([t for _, t in cfg_res.values()], pg, dev)
+
     flops = prefill_flops(wp, feat.get("prefix_len", 0))
     kvb = decode_kv_bytes(wd, feat.get("prefix_len", 0))
     t_pre, t_dec, t_all, te_pre, te_dec = max_over_ranks([t_pre, t_dec, t_all, te_pre, te_dec], pg, dev)
@@ -537,6 +556,26 @@ def run_ours(args):
             if not do_pre:
                 line["value"], line["unit"] = line["decode"]["value"], "GB/s"
                 e2e.update({"value": e2e["decode_value"], "unit": "GB/s"})
+        if cfg_res:
+            configs = {}
+            for (name, (w, _)), t in zip(cfg_res.items(), cfg_t):
+                fl = prefill_flops(w)
+                ach = fl / t / 1e12
+                kname = prefill_kernel_name(w)
+                configs[name] = {
+                    "workload": "B%d Hq%d Hkv%d S%d d%d%s W%d" % (
+                        w.B, w.H_q, w.H_kv, w.S_q, w.d_h, ("+%d decoupled RoPE" % w.d_r) if w.d_r else "",
+                        w.window),
+                    "ms_per_call": t * 1e3, "tflop_per_call": fl / 1e12,
+                    "value": world * fl / t / 1e12, "unit": "TFLOP/s", "calls": K,
+                    "roofline": {"kernel": kname, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                                 "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
+                                 "frac_of_bf16_sustained": ach / peaks["bf16_tflops_sustained"],
+                                 "traffic": traffic.get("prefill_" + name +
+                                                        ("_single" if kname == "prefill_kernel" else "")),
+                                 "peak_source": peaks["source"] + " (burst)"}}
+            line["configs"] = configs
+            line["configs_clocks"] = cfg_clocks
         # the kernel that dominates the step's time carries the roofline key
         if do_dec and (not do_pre or t_dec >= t_pre):
             line["roofline"] = line["roofline_decode"]
@@ -552,6 +591,89 @@ def run_ours(args):
     if pg:
         pg.barrier()
         pg.destroy_process_group()
+    return 0
+
+
+def prefill_call(apex, w, q, k, v, out, feat):
+    if w.d_r:
+        return apex.mla_fwd(q, k, v, w.d_r, window=w.window, q_pos0=w.q_pos0, rope_base=w.rope_base, out=out,
+                            **feat)
+    return apex.fwd(q, k, v, window=w.window, q_pos0=w.q_pos0, rope_base=w.rope_base, out=out, **feat)
+
+
+def prefill_kernel_name(w):
+    if not w.d_r and (w.d_h != 128 or os.environ.get("APEX_ATTN_PREFILL") == "single"):
+        return "prefill_kernel"
+    return "prefill_pair_kernel"
+
+
+def time_prefill_configs(names, rank, K, warm, stream, dev):
+    """Each named prefill workload on its own: W warm-up calls, then K calls with
+    CUDA events around each on the launching stream; returns seconds per call."""
+    import torch
+
+    import transformer_attention_rope_gb300 as apex
+    from transformer_attention_rope_gb300 import inputs as inp
+    res = {}
+    for name in names:
+        w = inp.WORKLOADS[name]
+        w = dataclasses.replace(w, seed=w.seed + 1000 * rank)
+        q, k, v = (t.to(dev) for t in inp.workload_inputs(w))
+        out = torch.empty((w.B, w.H_q, w.S_q, w.d_h), dtype=torch.bfloat16, device=dev)
+        apex.apex_attn_rope_reserve(w.S_k, w.d_r or w.d_h, w.rope_base)
+        for _ in range(warm):
+            prefill_call(apex, w, q, k, v, out, {})
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for a, b in ev:
+            a.record(stream)
+            prefill_call(apex, w, q, k, v, out, {})
+            b.record(stream)
+        torch.cuda.synchronize()
+        res[name] = (w, sum(a.elapsed_time(b) for a, b in ev) / 1e3 / K)
+        del q, k, v, out
+        torch.cuda.empty_cache()
+    st = apex.apex_attn_device_status()
+    if st != 0:
+        raise RuntimeError("device status %d after the prefill configs" % st)
+    return res
+
+
+def free_port():
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_ranks(n, argv):
+    """Start n ranks of this script under torch.distributed.run (one node,
+    rendezvous on 127.0.0.1) and return the launcher's exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(n),
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
+def run_launcher_check(args):
+    """Host logic of the N-rank bench without a GPU: gloo process group, the
+    per-rank seeds, and the max-over-ranks reduction of the timings."""
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("gloo")
+    wp, wd = rank_workloads(rank, args.prefill_workload, args.decode_batch, args.decode_workload)
+    timings = max_over_ranks([1.0 + rank, 2.0 * (world - rank)], dist if world > 1 else None)
+    seeds = [[wp.seed, wd.seed]]
+    if world > 1:
+        gathered = [None] * world
+        dist.all_gather_object(gathered, [wp.seed, wd.seed])
+        seeds = gathered
+    if rank == 0:
+        print(json.dumps({"launcher_check": True, "n_ranks": world, "gpus_flag": args.gpus, "seeds": seeds,
+                          "max_over_ranks": timings, "local_rank": local}))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
     return 0
 
 
@@ -595,7 +717,36 @@ def main():
                     help="run the step with one of the block's options")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="decode batch size (profiling a smaller case; default: the workload's 64)")
+    ap.add_argument("--configs", default=None,
+                    help="comma list of further prefill workloads timed after the step (wide, long, mla) or "
+                         "'none'; default: all three with --part all and --feature none, else none")
+    ap.add_argument("--launcher-check", action="store_true",
+                    help="start the ranks and run only their host logic (gloo, no GPU)")
     args = ap.parse_args()
+    if args.configs is None:
+        args.configs = "wide,long,mla" if (args.part == "all" and args.feature == "none") else "none"
+    names = [c for c in args.configs.split(",") if c and c != "none"]
+    for c in names:
+        if c not in ("tiny", "gqa", "wide", "long", "mla"):
+            ap.error("unknown prefill workload in --configs: %s" % c)
+    args.config_names = names
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if "WORLD_SIZE" in os.environ:
+        if int(os.environ["WORLD_SIZE"]) != args.gpus:
+            print("bench.py: WORLD_SIZE=%s but --gpus %d" % (os.environ["WORLD_SIZE"], args.gpus), file=sys.stderr)
+            return 2
+    elif args.gpus > 1:
+        # no launcher around us: start the N ranks ourselves
+        if not args.launcher_check and args.impl == "ours":
+            import torch
+            have = torch.cuda.device_count()
+            if have < args.gpus:
+                print("bench.py: --gpus %d but %d GPU(s) visible" % (args.gpus, have), file=sys.stderr)
+                return 2
+        return launch_ranks(args.gpus, sys.argv[1:])
+    if args.launcher_check:
+        return run_launcher_check(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -250,9 +250,11 @@ apex_status apex_attn_decode(const void *q, const void *k_cache, const void *v_c
  *     capturing any CUDA graph.
  *   Concurrency: all calls on a device share the arrays, so calls that may
  *     overlap on the GPU (different streams without ordering between them) race
- *     and must not be issued.  A kernel wait that times out is not recorded
- *     (there is no status word without allocation); the output is then
- *     unspecified.
+ *     and must not be issued.  Kernel waits are bounded as on the other entry
+ *     points (APEX_ATTN_WAIT_TIMEOUT_MS, 2 s by default), but a wait that times
+ *     out is not recorded (there is no status word without allocation); the
+ *     output is then unspecified.  If the table build fails (APEX_ERR_CUDA),
+ *     the next call rebuilds it.
  */
 apex_status apex_attn_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, void *out,
                                      int B, int H_q, int H_kv, int S_k, int d_h, int window, int q_pos,

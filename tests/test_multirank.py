@@ -53,3 +53,43 @@ def test_two_gloo_ranks_reduce_times_and_split_seeds():
 
 def test_single_rank_needs_no_process_group():
     assert bench.max_over_ranks([3.0, 4.0], None) == [3.0, 4.0]
+
+
+def _bench(args, env_extra=None, timeout=300):
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    env.update(env_extra or {})
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py")] + args, cwd=root, env=env,
+                         capture_output=True, text=True, timeout=timeout)
+    lines = [json.loads(l) for l in out.stdout.splitlines() if l.startswith("{")]
+    return out.returncode, lines, out.stderr
+
+
+def test_bench_gpus_flag_starts_its_own_ranks():
+    """`bench.py --gpus 2` with no launcher around it starts two ranks itself
+    (gloo here, no GPU): rank 0 prints one line with both ranks' seeds and the
+    max-over-ranks timings."""
+    rc, lines, err = _bench(["--gpus", "2", "--launcher-check"])
+    assert rc == 0, err[-2000:]
+    assert len(lines) == 1, lines
+    d = lines[0]
+    assert d["n_ranks"] == 2 and d["gpus_flag"] == 2
+    assert d["seeds"] == [[1, 4], [1001, 1004]]
+    assert d["max_over_ranks"] == [2.0, 4.0]
+
+
+def test_bench_refuses_more_gpus_than_visible():
+    rc, lines, err = _bench(["--gpus", "2", "--steps", "1"])
+    assert rc == 2 and not lines
+    assert "GPU(s) visible" in err
+
+
+def test_bench_refuses_world_size_mismatch():
+    rc, lines, err = _bench(["--gpus", "4", "--launcher-check"], {"WORLD_SIZE": "2", "RANK": "0"})
+    assert rc == 2 and not lines
+    assert "WORLD_SIZE" in err

@@ -174,17 +174,51 @@ def _sample_rows(w, n_rand=48):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["gqa", "wide", "long"])
-def test_prefill_full_workload_sampled_rows(name):
+def _item_rows(w):
+    """One seeded row in each of the four M tiles of every work item of the
+    CTA-pair prefill kernel (an item is 4 * 128 / G consecutive query rows of
+    one (batch, KV head) unit; tile T of it holds rows T * 128 / G onwards, the
+    G heads of each row packed into one 128-row tile), so every item -- the
+    first of a unit, the middle ones, the last and ragged one, those whose
+    window starts in another key tile -- and both CTAs' tiles are checked in
+    every (batch, KV head) unit; plus the rows of _sample_rows."""
+    P = 128 // w.G
+    rng = np.random.default_rng(10_000 + w.seed)
+    rows = set(_sample_rows(w))
+    for r0 in range(0, w.S_q, 4 * P):
+        for T in range(4):
+            lo = r0 + T * P
+            if lo < w.S_q:
+                rows.add(int(rng.integers(lo, min(lo + P, w.S_q))))
+    return sorted(rows)
+
+
+def test_prefill_gqa_full_workload_every_row():
+    """The gqa workload in the bench's launch configuration, every output
+    element of every (batch, head, row) against the oracle."""
+    dev = _dev()
+    w = inputs.WORKLOADS["gqa"]
+    q, k, v = inputs.workload_inputs(w)
+    out = apex.fwd(q.to(dev), k.to(dev), v.to(dev), window=w.window, q_pos0=w.q_pos0)
+    torch.cuda.synchronize()
+    ref = oracle.attn(q, k, v, window=w.window, q_pos0=w.q_pos0)
+    _assert_close(out, ref, "gqa")
+    _status_ok()
+
+
+@pytest.mark.parametrize("name", ["wide", "long"])
+def test_prefill_full_workload_every_item(name):
     """Full-size workloads in the launch configuration the bench times; the oracle
-    checks a sample of rows of every (batch, head): the first and last 64, the
-    window edge and random rows."""
+    checks every head of a row set that touches every work item and both tiles of
+    each CTA of the pair kernel, plus the first and last 64 rows, the window edge
+    and random rows."""
     dev = _dev()
     w = inputs.WORKLOADS[name]
     q, k, v = inputs.workload_inputs(w)
     out = apex.fwd(q.to(dev), k.to(dev), v.to(dev), window=w.window, q_pos0=w.q_pos0)
     torch.cuda.synchronize()
-    rows = _sample_rows(w)
+    rows = _item_rows(w)
+    assert len(rows) >= w.S_q // (128 // w.G)
     ref = oracle.attn(q, k, v, window=w.window, q_pos0=w.q_pos0, rows=rows)
     _assert_close(out[:, :, rows], ref, name)
     _status_ok()

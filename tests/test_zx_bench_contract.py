@@ -25,7 +25,7 @@ def _run(args):
 def test_device_arm_json_contract():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    d = _run(["--steps", "2", "--warmup", "3", "--decode-batch", "2"])
+    d = _run(["--steps", "2", "--warmup", "3", "--decode-batch", "2", "--configs", "wide"])
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
                 "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
         assert key in d, key
@@ -46,6 +46,11 @@ def test_device_arm_json_contract():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1
     assert d["gpu_launches"] == 3 * d["steps"]  # prefill + decode split + combine per step
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    c = d["configs"]["wide"]
+    for key in ("workload", "ms_per_call", "value", "unit", "roofline"):
+        assert key in c, key
+    assert c["roofline"]["bound"] == "tensor" and c["roofline"]["frac"] > 0
+    assert abs(c["roofline"]["frac"] - c["roofline"]["achieved"] / c["roofline"]["peak"]) < 1e-9
 
 
 def test_reference_arm_json_contract():

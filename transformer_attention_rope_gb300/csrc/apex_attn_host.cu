@@ -15,6 +15,18 @@
 #include "kernel_params.h"
 
 namespace apex {
+
+uint64_t wait_timeout_ns()
+{
+    static uint64_t v = [] {
+        const char *e = getenv("APEX_ATTN_WAIT_TIMEOUT_MS");
+        long ms = e ? atol(e) : 0;
+        if (ms <= 0) ms = 2000;
+        return (uint64_t)ms * 1000000ull;
+    }();
+    return v;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -53,17 +65,6 @@ struct DeviceState {
 };
 
 DeviceState g_state[kMaxDevices];
-
-uint64_t wait_timeout_ns()
-{
-    static uint64_t v = [] {
-        const char *e = getenv("APEX_ATTN_WAIT_TIMEOUT_MS");
-        long ms = e ? atol(e) : 0;
-        if (ms <= 0) ms = 2000;
-        return (uint64_t)ms * 1000000ull;
-    }();
-    return v;
-}
 
 // Prefill kernel choice for the plain block: the CTA-pair kernel for d_h = 128
 // (measured 12 % faster than the single-CTA kernel on the B4 H_q32 H_kv8 S4096

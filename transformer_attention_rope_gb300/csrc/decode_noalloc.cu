@@ -142,7 +142,11 @@ extern "C" apex_status apex_attn_decode_noalloc(const void *q, const void *k_cac
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (st.table_d != d_h || st.table_base != rope_base) {
-        // (re)build the RoPE table for this (d_h, base), in stream order
+        // (re)build the RoPE table for this (d_h, base), in stream order.  The
+        // key is cleared first: if the launch or the wait fails, the array holds
+        // a partly rewritten table that no later call may take for a valid one.
+        st.table_d = 0;
+        st.table_base = 0.f;
         rope_table_kernel<<<st.sm_count * 4, 256, 0, s>>>(st.rope, d_h, (double)rope_base);
         if (cudaGetLastError() != cudaSuccess) return APEX_ERR_CUDA;
         // finished before any later call, on any stream, reads it
@@ -160,7 +164,7 @@ extern "C" apex_status apex_attn_decode_noalloc(const void *q, const void *k_cac
     p.q = static_cast<const uint16_t *>(q);
     p.out = static_cast<uint16_t *>(out);
     p.rope = RopeTableView{st.rope, kMaxPos};
-    p.wait = WaitCtl{nullptr, 2000000000ull};
+    p.wait = WaitCtl{nullptr, wait_timeout_ns()};  // no status word: a time-out is not recorded
     p.B = B;
     p.H_q = H_q;
     p.H_kv = H_kv;

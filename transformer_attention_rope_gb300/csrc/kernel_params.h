@@ -16,6 +16,10 @@ struct WaitCtl {
     uint64_t timeout_ns;  // bound on any single wait
 };
 
+// Bound on a single kernel wait: APEX_ATTN_WAIT_TIMEOUT_MS milliseconds when
+// that variable holds a positive number, else 2 s (read once per process).
+uint64_t wait_timeout_ns();
+
 // (cos, sin)(pos * theta_i) for pos in [0, max_pos), i in [0, d_h/2), fp32,
 // row-major [max_pos][d_h/2].
 struct RopeTableView {

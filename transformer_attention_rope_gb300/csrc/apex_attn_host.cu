@@ -199,6 +199,24 @@ bool make_map(CUtensorMap *m, const void *base, int d_h, int rows, int outer, in
     return r == CUDA_SUCCESS;
 }
 
+// 4-D bf16 map over the output [units][G][S_q][128] of the CTA-pair prefill,
+// box {64, min(P, 32), max(1, 32 / P), 1} with P = 128 / G (the 32 M-tile rows of
+// one softmax warp, head-major), 128-byte swizzle.
+bool make_out_map(CUtensorMap *m, void *base, int S_q, int G, int units)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const int P = 128 / G;
+    cuuint64_t dims[4] = {128, (cuuint64_t)S_q, (cuuint64_t)G, (cuuint64_t)units};
+    cuuint64_t strides[3] = {256, (cuuint64_t)S_q * 256, (cuuint64_t)G * S_q * 256};
+    cuuint32_t box[4] = {64, (cuuint32_t)std::min(P, 32), (cuuint32_t)std::max(1, 32 / P), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool supported_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16; }
@@ -484,6 +502,7 @@ apex_status prefill_launch(const void *q, const void *k, const void *v, void *ou
         !make_map(&L.tm_k, k, d_qk, S_k, B * H_kv, pair ? 64 : 128, 1) ||
         !make_map(&L.tm_v, v, d_v, S_k, B * H_kv, 128, 1))
         return APEX_ERR_CUDA;
+    if (pair && (d_v != 128 || !make_out_map(&L.tm_o, out, S_q, G, B * H_kv))) return APEX_ERR_CUDA;
     PrefillParams &p = L.p;
     p.out = static_cast<uint16_t *>(out);
     p.rope = tv;

@@ -118,6 +118,27 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
+// 4-D tiled store shared -> global, tracked by the issuing thread's bulk groups;
+// elements of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *m, uint32_t src, int x, int y, int z, int w)
+{
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// The thread's committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// The thread's committed bulk stores have completed (writes performed).
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---------------------------------------------------------------- warp MMA
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr)
 {
@@ -219,8 +240,8 @@ __device__ __forceinline__ float fast_exp2(float x)
 
 // Launch a prefill kernel as a programmatic dependent of the stream's previous
 // work (its blocks wait in griddepcontrol.wait before touching global memory).
-template <typename K, typename L>
-inline cudaError_t launch_dependent(K kernel, int grid, int threads, int smem, cudaStream_t stream, const L &l)
+template <typename K, typename... A>
+inline cudaError_t launch_dependent(K kernel, int grid, int threads, int smem, cudaStream_t stream, const A &...args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -232,7 +253,7 @@ inline cudaError_t launch_dependent(K kernel, int grid, int threads, int smem, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, l.tm_q, l.tm_k, l.tm_v, l.p);
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // Sets to -inf the scores of a 128-key row that lie outside the row's visible

@@ -81,6 +81,11 @@ struct PrefillParams {
 
 struct PrefillLaunch {
     CUtensorMap tm_q, tm_k, tm_v;
+    // CTA-pair kernel: 4-D map over out viewed as [B*H_kv][G][S_q][128] (the G
+    // query heads of a KV head adjacent), box {64, min(P, 32), max(1, 32 / P), 1}
+    // with P = 128 / G: one box is the 64-dim half of the 32 M-tile rows of one
+    // warp; 128-byte swizzle; elements outside the tensor are not written
+    CUtensorMap tm_o;
     PrefillParams p;
     int grid;  // persistent CTAs (at most one per SM)
 };

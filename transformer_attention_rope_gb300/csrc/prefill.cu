@@ -576,7 +576,7 @@ cudaError_t launch_t(const PrefillLaunch &L, cudaStream_t stream)
     err = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
     if (err != cudaSuccess) return err;
     if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-    return launch_dependent(prefill_kernel<D>, L.grid, kThreads, C::kSmemBytes, stream, L);
+    return launch_dependent(prefill_kernel<D>, L.grid, kThreads, C::kSmemBytes, stream, L.tm_q, L.tm_k, L.tm_v, L.p);
 }
 
 }  // namespace

@@ -60,13 +60,20 @@ struct PairCfg {
     static constexpr int kVStages = kStages;  // K(x) and V(x) share stage x % kStages and one "empty" barrier
     static constexpr int kQTile = kBoxes * kQBox;     // 128 rows x DQK
     static constexpr int kKTile = kBoxes * kKBox;     // this CTA's 64 keys x DQK
-    // Q | V stages | K stages | 8 KB guard | barriers: an operand descriptor that
-    // walked past its tile (it should not: each CTA's B half is 64 rows or 64
-    // columns) would still stay inside the allocation.
+    // O leaves through shared memory and TMA stores where there is room for the
+    // staging buffers (128-wide rows); the 192-wide rows keep per-thread stores.
+    static constexpr bool kTmaStoreO = DQK == 128;
+    static constexpr int kStageWarpBytes = 32 * DV * 2;  // one softmax warp's 32 rows of O, bf16
+    // Q | V stages | K stages | O staging (8 softmax warps) or 8 KB guard |
+    // barriers: an operand descriptor that walked past its tile (it should not:
+    // each CTA's B half is 64 rows or 64 columns) would still stay inside the
+    // allocation.
     static constexpr int kQOff = 0;
     static constexpr int kVOff = 2 * kQTile;
     static constexpr int kKOff = kVOff + kVStages * kVTile;
-    static constexpr int kBarOff = kKOff + kKStages * kKTile + 8192;
+    static constexpr int kStageOff = kKOff + kKStages * kKTile;
+    static constexpr int kBarOff = kStageOff + (kTmaStoreO ? 8 * kStageWarpBytes : 8192);
+    static_assert(kStageOff % 1024 == 0, "staging buffers need 1024-byte alignment for the 128-byte swizzle");
     // barrier slots
     static constexpr int kBarQFull = 0;                         // [2]  local TMA
     static constexpr int kBarQReady = 2;                        // [2]  leader: 8 warps (both CTAs)
@@ -324,7 +331,8 @@ __device__ __forceinline__ int item_index(int k)
 template <int DQK, int DR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p)
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                        const PrefillParams p)
 {
     using C = PairCfg<DQK, DR>;
     constexpr int kKStages = C::kKStages, kVStages = C::kVStages;
@@ -385,6 +393,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
+            if (C::kTmaStoreO) tma_prefetch_desc(&tm_o);
             int kc = 0;
             for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
                 const Item it = make_item(p, w);
@@ -629,25 +638,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             pair_wait(bar(kBarODone + t), k & 1, p.wait, abort);
             tc_fence_after();
             const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-            const int hl = i / P;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(it.zq + hl) * p.S_q + r) * DV);
+            if constexpr (C::kTmaStoreO) {
+                // The warp's 32 rows go to its staging buffer as two swizzled
+                // [32 rows][64 dims] boxes (box row == lane: rows are head-major,
+                // P positions per head), then leave by two TMA stores; rows past
+                // S_q fall outside the tensor and are not written.
+                uint8_t *stage = smem + C::kStageOff + warp * C::kStageWarpBytes;
+                if (lane == 0) bulk_wait_group_read0();  // the previous item's stores have read it
+                __syncwarp();
 #pragma unroll
-            for (int ch = 0; ch < DV / 32; ++ch) {
-                uint32_t o[32];
-                tmem_ld32(o_addr + 32 * ch, o);
-                tmem_wait_ld();
-                uint32_t w2[16];
+                for (int ch = 0; ch < DV / 32; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld32(o_addr + 32 * ch, o);
+                    tmem_wait_ld();
+                    uint32_t w2[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w2[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-                if (r < p.S_q) {
+                    for (int e = 0; e < 16; ++e)
+                        w2[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                    uint8_t *half = stage + (ch >> 1) * (C::kStageWarpBytes / 2);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4)
-                        dst[4 * ch + q4] = make_uint4(w2[4 * q4], w2[4 * q4 + 1], w2[4 * q4 + 2], w2[4 * q4 + 3]);
+                        *reinterpret_cast<uint4 *>(half + swz128(lane, (ch & 1) * 4 + q4)) =
+                            make_uint4(w2[4 * q4], w2[4 * q4 + 1], w2[4 * q4 + 2], w2[4 * q4 + 3]);
                 }
+                tc_fence_before();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int wq = 32 * (warp & 3);          // the warp's first M-tile row
+                    const int y = it.r0 + T * P + wq % P;    // its output row (query index)
+                    if (y < p.S_q) {
+                        tma_store_4d(&tm_o, smem_u32(stage), 0, y, wq / P, it.unit);
+                        tma_store_4d(&tm_o, smem_u32(stage) + C::kStageWarpBytes / 2, 64, y, wq / P, it.unit);
+                    }
+                    bulk_commit_group();
+                }
+            } else {
+                const int hl = i / P;
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(it.zq + hl) * p.S_q + r) * DV);
+#pragma unroll
+                for (int ch = 0; ch < DV / 32; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld32(o_addr + 32 * ch, o);
+                    tmem_wait_ld();
+                    uint32_t w2[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w2[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                    if (r < p.S_q) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            dst[4 * ch + q4] =
+                                make_uint4(w2[4 * q4], w2[4 * q4 + 1], w2[4 * q4 + 2], w2[4 * q4 + 3]);
+                    }
+                }
+                tc_fence_before();
             }
-            tc_fence_before();
         }
+        // the last item's stores have completed before the CTA (and its shared memory) goes
+        if (C::kTmaStoreO && lane == 0) bulk_wait_group0();
     }
 
     __syncwarp();
@@ -672,7 +721,8 @@ cudaError_t launch_pair_t(const PrefillLaunch &L, cudaStream_t stream)
     err = cudaFuncGetAttributes(&fa, prefill_pair_kernel<DQK, DR>);
     if (err != cudaSuccess) return err;
     if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-    return launch_dependent(prefill_pair_kernel<DQK, DR>, L.grid, kThreads, C::kSmemBytes, stream, L);
+    return launch_dependent(prefill_pair_kernel<DQK, DR>, L.grid, kThreads, C::kSmemBytes, stream, L.tm_q, L.tm_k,
+                            L.tm_v, L.tm_o, L.p);
 }
 
 }  // namespace

@@ -533,13 +533,14 @@ def run_ours(args):
             line["prefill"] = {"value": line["value"], "unit": "TFLOP/s", "ms_per_call": pre_launch_s * 1e3,
                                "frac_of_bf16": pre_achieved / peaks["bf16_tflops"],
                                "frac_of_bf16_sustained": pre_achieved / peaks["bf16_tflops_sustained"]}
-            kname = "prefill_kernel" if (not wp.d_r and (wp.d_h != 128 or os.environ.get("APEX_ATTN_PREFILL")
-                                                                 == "single")) else "prefill_pair_kernel"
-            line["roofline_prefill"] = {"kernel": kname, "bound": "tensor", "achieved": pre_achieved,
+            kname, prerot = prefill_kernel_name(wp, feat)
+            line["roofline_prefill"] = {"kernel": kernel_label(kname, prerot), "bound": "tensor",
+                                        "achieved": pre_achieved,
                                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                         "frac": pre_achieved / peaks["bf16_tflops"],
-                                        "traffic": traffic.get("prefill_" + wp.name +
-                                                               ("_single" if kname == "prefill_kernel" else "")),
+                                        "traffic": call_traffic(traffic, "prefill_" + wp.name +
+                                                                ("_single" if kname == "prefill_kernel" else ""),
+                                                                prerot),
                                         "peak_source": peaks["source"] + " (burst)"}
             e2e.update({"value": world * K * flops / te_pre / 1e12, "unit": "TFLOP/s"})
         if do_dec:
@@ -561,18 +562,19 @@ def run_ours(args):
             for (name, (w, _)), t in zip(cfg_res.items(), cfg_t):
                 fl = prefill_flops(w)
                 ach = fl / t / 1e12
-                kname = prefill_kernel_name(w)
+                kname, prerot = prefill_kernel_name(w)
                 configs[name] = {
                     "workload": "B%d Hq%d Hkv%d S%d d%d%s W%d" % (
                         w.B, w.H_q, w.H_kv, w.S_q, w.d_h, ("+%d decoupled RoPE" % w.d_r) if w.d_r else "",
                         w.window),
                     "ms_per_call": t * 1e3, "tflop_per_call": fl / 1e12,
                     "value": world * fl / t / 1e12, "unit": "TFLOP/s", "calls": K,
-                    "roofline": {"kernel": kname, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                    "roofline": {"kernel": kernel_label(kname, prerot), "bound": "tensor", "achieved": ach,
+                                 "peak": peaks["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
                                  "frac_of_bf16_sustained": ach / peaks["bf16_tflops_sustained"],
-                                 "traffic": traffic.get("prefill_" + name +
-                                                        ("_single" if kname == "prefill_kernel" else "")),
+                                 "traffic": call_traffic(traffic, "prefill_" + name +
+                                                         ("_single" if kname == "prefill_kernel" else ""), prerot),
                                  "peak_source": peaks["source"] + " (burst)"}}
             line["configs"] = configs
             line["configs_clocks"] = cfg_clocks
@@ -582,7 +584,8 @@ def run_ours(args):
         else:
             line["roofline"] = line["roofline_prefill"]
         line["e2e"] = e2e
-        line["gpu_launches"] = K * ((1 if do_pre else 0) + (2 if do_dec else 0))
+        pre_launches = (2 if prefill_kernel_name(wp, feat)[1] else 1) if do_pre else 0
+        line["gpu_launches"] = K * (pre_launches + (2 if do_dec else 0))
         line["clocks"] = clocks
         line["wall_s_timed"] = t_wall
         if cpu is not None:
@@ -601,10 +604,33 @@ def prefill_call(apex, w, q, k, v, out, feat):
     return apex.fwd(q, k, v, window=w.window, q_pos0=w.q_pos0, rope_base=w.rope_base, out=out, **feat)
 
 
-def prefill_kernel_name(w):
+def prefill_kernel_name(w, feat=None):
+    """The prefill kernel a call runs, and whether the keys are rotated once by
+    rope_keys_kernel before it (the call's time covers both)."""
     if not w.d_r and (w.d_h != 128 or os.environ.get("APEX_ATTN_PREFILL") == "single"):
-        return "prefill_kernel"
-    return "prefill_pair_kernel"
+        return "prefill_kernel", False
+    if w.d_r:
+        return "prefill_pair_kernel", False
+    import transformer_attention_rope_gb300 as apex
+    opts = {k: v for k, v in (feat or {}).items()}
+    prerot = apex.fwd_workspace_bytes(w.B, w.H_q, w.H_kv, w.S_q, w.S_k, w.d_h, window=w.window, q_pos0=w.q_pos0,
+                                      rope_base=w.rope_base, **opts) > 0
+    return "prefill_pair_kernel", prerot
+
+
+def call_traffic(traffic, key, prerot):
+    """DRAM bytes of one call: the prefill kernel's, plus the key-rotation pass's
+    when it runs (null when either capture is missing or stale)."""
+    a = traffic.get(key)
+    if not prerot:
+        return a
+    b = traffic.get(key + "_rope_keys")
+    return a + b if (a is not None and b is not None) else None
+
+
+def kernel_label(name, prerot):
+    return ("rope_keys_kernel + %s (keys rotated once into the workspace, then the prefill; timed together)" % name
+            if prerot else name)
 
 
 def time_prefill_configs(names, rank, K, warm, stream, dev):

@@ -118,6 +118,42 @@ apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *
                              const apex_attn_options *opt, apex_stream_t stream);
 
 /*
+ * Bytes of caller-provided device workspace apex_attn_fwd_ws will use for this
+ * call (same arguments): one rotated copy of the keys, B * H_kv * S_k * d_h bf16
+ * values, when the library's cost model rotates the keys before the prefill;
+ * 0 when it would not (then no workspace is needed), when opt->keys_prerotated
+ * is set, and when the arguments are invalid.  Host-only, no CUDA call.
+ */
+size_t apex_attn_fwd_workspace_bytes(int B, int H_q, int H_kv, int S_q, int S_k, int d_h,
+                                     const apex_attn_options *opt);
+
+/*
+ * Prefill with options and a workspace: the same result as apex_attn_fwd_ex
+ * (same arguments, layouts, masks and rounding up to the order of fp32 sums),
+ * computed faster on long or wide problems.  The pages rotate every key by its
+ * position (Part 1 §4.2-§4.5); the prefill rotates each 128-key tile in shared
+ * memory once for every work item that reaches it, which on long windows or
+ * wide head groups means tens of times.  Given a workspace, the library may
+ * instead rotate the keys once, RoPE(k_j, j) in bf16 as apex_attn_rope_keys
+ * computes it, into the workspace and run the prefill on those (it does so when
+ * its cost model -- key-tile visits against one read and write of K -- says
+ * that is faster; otherwise the workspace is left untouched).
+ *
+ *   workspace, workspace_bytes: NULL (then this is apex_attn_fwd_ex), or device
+ *     memory of at least apex_attn_fwd_workspace_bytes(...) bytes for the same
+ *     arguments, 16-byte aligned, owned by the caller, not overlapping q, k, v
+ *     or out, not read before written; a smaller or misaligned workspace gives
+ *     APEX_ERR_INVALID_ARG before any launch.
+ *   The pass is a second kernel on `stream` before the prefill; with
+ *   opt->keys_prerotated, or on the single-CTA kernel (d_h = 64), no pass runs.
+ * Errors as for apex_attn_fwd_ex.
+ */
+apex_status apex_attn_fwd_ws(const void *q, const void *k, const void *v, void *out,
+                             int B, int H_q, int H_kv, int S_q, int S_k, int d_h,
+                             const apex_attn_options *opt, void *workspace, size_t workspace_bytes,
+                             apex_stream_t stream);
+
+/*
  * Prefill of multi-head latent attention with decoupled RoPE (Part 2 §9.3):
  * query and key rows are [content | rope part], the rope part alone is
  * rotated, and values keep the content length.

@@ -121,6 +121,35 @@ def test_fwd_ex_rejects(lib, shape, opt, code):
     assert apex.apex_attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, *shape, o, None) == code
 
 
+# prefill with a workspace: (B, H_q, H_kv, S_q, S_k, d_h), options, workspace, bytes, expected status
+@pytest.mark.parametrize("shape,opt,ws,nbytes,code", [
+    ((1, 4, 2, 8, 8, 128), None, FAKE, 1 << 20, 1),                 # no options
+    ((1, 4, 2, 8, 8, 128), {}, FAKE + 8, 1 << 20, 1),               # misaligned workspace
+    ((1, 128, 8, 8192, 8192, 128), {}, FAKE, 8 * 8192 * 128 * 2 - 16, 1),  # one row short of the keys
+    ((1, 4, 2, 8, 8, 128), dict(q_pos=1), FAKE, 1 << 20, 1),        # q_pos0 + S_q > S_k
+    ((1, 4, 2, 8, 8, 96), {}, FAKE, 1 << 20, 2),                    # d_h = 96
+    ((1, 3, 2, 8, 8, 128), {}, FAKE, 1 << 20, 1),                   # H_q % H_kv != 0
+])
+def test_fwd_ws_rejects(lib, shape, opt, ws, nbytes, code):
+    o = None if opt is None else _opt(**opt)
+    assert apex.apex_attn_fwd_ws(FAKE, FAKE, FAKE, FAKE, *shape, o, ws, nbytes, None) == code
+
+
+def test_fwd_workspace_bytes(lib):
+    # one bf16 copy of the keys where the pass pays (long windows, wide head groups) ...
+    for shape, window in (((4, 32, 8, 4096, 4096, 128), 1024), ((1, 128, 8, 8192, 8192, 128), 0),
+                          ((1, 32, 8, 65536, 65536, 128), 4096)):
+        B, H_q, H_kv, S_q, S_k, d = shape
+        assert apex.fwd_workspace_bytes(*shape, window=window) == B * H_kv * S_k * d * 2
+    # ... none for small problems, pre-rotated keys, d_h = 64 (single-CTA kernel) or bad sizes
+    assert apex.fwd_workspace_bytes(1, 4, 2, 256, 256, 128) == 0
+    assert apex.fwd_workspace_bytes(4, 32, 8, 4096, 4096, 128, window=1024, keys_prerotated=True) == 0
+    assert apex.fwd_workspace_bytes(4, 32, 8, 4096, 4096, 64, window=1024) == 0
+    assert apex.fwd_workspace_bytes(1, 3, 2, 4096, 4096, 128) == 0
+    assert apex.fwd_workspace_bytes(1, 4, 2, 4096, 4000, 128) == 0   # S_q > S_k
+    assert apex.apex_attn_fwd_workspace_bytes(4, 32, 8, 4096, 4096, 128, None) == 0
+
+
 # decoupled-RoPE prefill: (B, H_q, H_kv, S_q, S_k, d_h, d_r), expected status
 @pytest.mark.parametrize("shape,code", [
     ((1, 4, 2, 8, 8, 128, 0), 1),

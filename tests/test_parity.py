@@ -194,15 +194,20 @@ def _item_rows(w):
 
 
 def test_prefill_gqa_full_workload_every_row():
-    """The gqa workload in the bench's launch configuration, every output
-    element of every (batch, head, row) against the oracle."""
+    """The gqa workload in the bench's launch configuration (keys rotated once
+    into a workspace first), and without a workspace (keys rotated in the
+    kernel): every output element of every (batch, head, row) against the
+    oracle."""
     dev = _dev()
     w = inputs.WORKLOADS["gqa"]
     q, k, v = inputs.workload_inputs(w)
-    out = apex.fwd(q.to(dev), k.to(dev), v.to(dev), window=w.window, q_pos0=w.q_pos0)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = apex.fwd(qd, kd, vd, window=w.window, q_pos0=w.q_pos0)
+    out2 = apex.fwd(qd, kd, vd, window=w.window, q_pos0=w.q_pos0, workspace=False)
     torch.cuda.synchronize()
     ref = oracle.attn(q, k, v, window=w.window, q_pos0=w.q_pos0)
     _assert_close(out, ref, "gqa")
+    _assert_close(out2, ref, "gqa, keys rotated in the kernel")
     _status_ok()
 
 

@@ -1,0 +1,103 @@
+"""GPU: prefill with a workspace (apex_attn_fwd_ws).  Where the library's cost
+model rotates the keys once into the workspace, the workspace must then hold
+exactly what apex_attn_rope_keys computes and the output must match the fp64
+oracle (and the in-kernel-rotation path within the parity tolerance); where it
+does not, the workspace is left untouched and the output is bit-identical to
+the call without a workspace.  Tolerance: max |err| <= 2e-2, mean |err| <= 2e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import transformer_attention_rope_gb300 as apex
+from transformer_attention_rope_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+MAX_ERR = 2e-2
+MEAN_ERR = 2e-3
+NAN_BF16 = -1  # 0xffff as int16: a NaN bf16 pattern no kernel writes
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def _errs(got, ref):
+    e = np.abs(torch.as_tensor(got).double().cpu().numpy() - np.asarray(ref, dtype=np.float64))
+    return float(e.max()), float(e.mean())
+
+
+def _ws(B, H_kv, S_k, d, dev):
+    n = B * H_kv * S_k * d * 2  # one bf16 copy of the keys
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    ws.view(torch.int16).fill_(NAN_BF16)
+    return ws
+
+
+def _rows(S, step):
+    return sorted(set(range(0, S, step)) | set(range(S - 64, S)) | set(range(64)))
+
+
+# shapes on which each key tile is visited often enough for the pass to run
+@pytest.mark.parametrize("B,H_q,H_kv,S,window,opts", [
+    (2, 8, 2, 8192, 4096, {}),                                   # G = 4, sliding window
+    (1, 32, 2, 8192, 0, {}),                                     # G = 16, causal
+    (2, 8, 2, 8192, 4096, dict(yarn_scale=8.0)),                 # YaRN frequencies in the pass
+    (1, 16, 4, 6000, 0, dict(prefix_len=700)),                   # prefix, ragged last tile
+])
+def test_pass_runs_and_matches_oracle(B, H_q, H_kv, S, window, opts):
+    dev = _dev()
+    d = 128
+    q, k, v = inputs.make_qkv(B, H_q, H_kv, S, S, d, 7700 + S + H_q)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    assert apex.fwd_workspace_bytes(B, H_q, H_kv, S, S, d, window=window, **opts) == B * H_kv * S * d * 2
+    ws = _ws(B, H_kv, S, d, dev)
+    out = apex.fwd(qd, kd, vd, window=window, workspace=ws, **opts)
+    torch.cuda.synchronize()
+    # the pass ran: the workspace holds the keys as apex_attn_rope_keys rotates them
+    rot = apex.rope_keys(kd, **{k_: v_ for k_, v_ in opts.items() if k_.startswith("yarn")})
+    held = ws.view(torch.bfloat16).view(B, H_kv, S, d)
+    assert torch.equal(held.view(torch.int16), rot.view(torch.int16))
+    rows = _rows(S, 7)
+    oracle_opts = {("yarn_s" if k_ == "yarn_scale" else k_): v_ for k_, v_ in opts.items()}
+    ref = oracle.attn(q, k, v, window=window, rows=rows, **oracle_opts)
+    mx, mean = _errs(out[:, :, rows].cpu(), ref)
+    assert mx <= MAX_ERR and mean <= MEAN_ERR, (mx, mean)
+    # and the in-kernel rotation path agrees within the tolerance
+    plain = apex.fwd(qd, kd, vd, window=window, workspace=False, **opts)
+    mx2, mean2 = _errs(out.cpu(), plain.double().cpu().numpy())
+    assert mx2 <= MAX_ERR and mean2 <= MEAN_ERR, (mx2, mean2)
+    assert apex.apex_attn_device_status() == 0
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,S,window", [
+    (1, 4, 2, 256, 0),
+    (2, 8, 2, 1000, 100),
+])
+def test_small_problem_leaves_workspace_untouched(B, H_q, H_kv, S, window):
+    dev = _dev()
+    d = 128
+    q, k, v = (t.to(dev) for t in inputs.make_qkv(B, H_q, H_kv, S, S, d, 7800 + S))
+    assert apex.fwd_workspace_bytes(B, H_q, H_kv, S, S, d, window=window) == 0
+    ws = _ws(B, H_kv, S, d, dev)
+    out = apex.fwd(q, k, v, window=window, workspace=ws)
+    ref = apex.fwd(q, k, v, window=window, workspace=False)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert bool((ws.view(torch.int16) == NAN_BF16).all())
+
+
+def test_prerotated_keys_never_use_the_workspace():
+    dev = _dev()
+    B, H_q, H_kv, S, d = 2, 8, 2, 8192, 128
+    q, k, v = (t.to(dev) for t in inputs.make_qkv(B, H_q, H_kv, S, S, d, 7900))
+    kr = apex.rope_keys(k)
+    ws = _ws(B, H_kv, S, d, dev)
+    out = apex.fwd(q, kr, v, window=2048, keys_prerotated=True, workspace=ws)
+    ref = apex.fwd(q, kr, v, window=2048, keys_prerotated=True, workspace=False)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert bool((ws.view(torch.int16) == NAN_BF16).all())

@@ -44,7 +44,9 @@ def test_device_arm_json_contract():
     for key in ("value", "unit", "cores", "kind", "sample"):
         assert key in cb, key
     assert cb["kind"] == "oracle" and cb["cores"] >= 1
-    assert d["gpu_launches"] == 3 * d["steps"]  # prefill + decode split + combine per step
+    # prefill (plus the key-rotation pass where it runs) + decode split + combine per step
+    pre = 2 if d["roofline_prefill"]["kernel"].startswith("rope_keys_kernel") else 1
+    assert d["gpu_launches"] == (pre + 2) * d["steps"]
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     c = d["configs"]["wide"]
     for key in ("workload", "ms_per_call", "value", "unit", "roofline"):

@@ -8,8 +8,8 @@ There is no CPU fallback -- if the library is missing, every call raises.
 Raw C-ABI names (pointers and sizes):
     apex_attn_fwd, apex_attn_decode, apex_attn_decode_noalloc, apex_attn_decode_workspace_bytes,
     apex_attn_rope_reserve, apex_attn_device_status, apex_attn_status_string,
-    apex_attn_fwd_ex, apex_attn_decode_ex, apex_attn_rope_keys, apex_attn_mla_fwd, apex_attn_mla_decode
-    (with an Options struct)
+    apex_attn_fwd_ex, apex_attn_fwd_ws, apex_attn_fwd_workspace_bytes, apex_attn_decode_ex, apex_attn_rope_keys,
+    apex_attn_mla_fwd, apex_attn_mla_decode (with an Options struct)
 Tensor conveniences (torch, bf16, contiguous, on the current CUDA device):
     fwd(q, k, v, ...), decode(q, k_cache, v_cache, q_pos, ...), rope_keys(k, ...), mla_fwd(q, k, v, d_r, ...),
     mla_decode(q, k_cache, v_cache, q_pos, d_r, ...)
@@ -23,7 +23,8 @@ import threading
 __all__ = [
     "ApexError", "library_path", "load_library", "apex_attn_fwd", "apex_attn_decode", "apex_attn_decode_noalloc",
     "apex_attn_decode_workspace_bytes", "apex_attn_rope_reserve", "apex_attn_device_status",
-    "apex_attn_status_string", "apex_attn_fwd_ex", "apex_attn_decode_ex", "apex_attn_rope_keys",
+    "apex_attn_status_string", "apex_attn_fwd_ex", "apex_attn_fwd_ws", "apex_attn_fwd_workspace_bytes",
+    "apex_attn_decode_ex", "apex_attn_rope_keys", "fwd_workspace_bytes",
     "apex_attn_mla_fwd", "apex_attn_mla_decode", "apex_attn_selftest_wait_timeout", "Options", "fwd", "decode",
     "decode_workspace_bytes",
     "rope_keys", "mla_fwd", "mla_decode",
@@ -76,6 +77,10 @@ def load_library():
             op = ctypes.POINTER(Options)
             lib.apex_attn_fwd_ex.argtypes = [vp, vp, vp, vp] + [i32] * 6 + [op, vp]
             lib.apex_attn_fwd_ex.restype = i32
+            lib.apex_attn_fwd_ws.argtypes = [vp, vp, vp, vp] + [i32] * 6 + [op, vp, sz, vp]
+            lib.apex_attn_fwd_ws.restype = i32
+            lib.apex_attn_fwd_workspace_bytes.argtypes = [i32] * 6 + [op]
+            lib.apex_attn_fwd_workspace_bytes.restype = sz
             lib.apex_attn_mla_fwd.argtypes = [vp, vp, vp, vp] + [i32] * 7 + [op, vp]
             lib.apex_attn_mla_fwd.restype = i32
             lib.apex_attn_mla_decode.argtypes = [vp, vp, vp, vp] + [i32] * 6 + [op, vp, sz, vp]
@@ -119,6 +124,17 @@ def apex_attn_decode_noalloc(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, w
 def apex_attn_fwd_ex(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, opt, stream) -> int:
     return load_library().apex_attn_fwd_ex(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h,
                                            ctypes.byref(opt) if opt is not None else None, stream)
+
+
+def apex_attn_fwd_ws(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, opt, workspace, workspace_bytes, stream) -> int:
+    return load_library().apex_attn_fwd_ws(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h,
+                                           ctypes.byref(opt) if opt is not None else None, workspace,
+                                           workspace_bytes, stream)
+
+
+def apex_attn_fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h, opt) -> int:
+    return load_library().apex_attn_fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h,
+                                                        ctypes.byref(opt) if opt is not None else None)
 
 
 def apex_attn_mla_fwd(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, d_r, opt, stream) -> int:
@@ -188,10 +204,24 @@ def _options(window=0, q_pos=0, rope_base=10000.0, yarn_scale=1.0, yarn_beta_fas
                    float(yarn_beta_slow), int(prefix_len), 1 if keys_prerotated else 0)
 
 
+def fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h, *, window: int = 0, q_pos0: int = 0,
+                        rope_base: float = 10000.0, yarn_scale: float = 1.0, yarn_beta_fast: float = 32.0,
+                        yarn_beta_slow: float = 1.0, prefix_len: int = 0, keys_prerotated: bool = False) -> int:
+    """Workspace bytes a prefill with these arguments uses (0: none; see apex_attn_fwd_workspace_bytes)."""
+    opt = _options(window, q_pos0, rope_base, yarn_scale, yarn_beta_fast, yarn_beta_slow, prefix_len,
+                   keys_prerotated)
+    return int(apex_attn_fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h, opt))
+
+
 def fwd(q, k, v, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.0, out=None, stream=None,
         yarn_scale: float = 1.0, yarn_beta_fast: float = 32.0, yarn_beta_slow: float = 1.0, prefix_len: int = 0,
-        keys_prerotated: bool = False):
-    """Prefill. q [B,H_q,S_q,d], k/v [B,H_kv,S_k,d] (bf16, CUDA) -> out [B,H_q,S_q,d]."""
+        keys_prerotated: bool = False, workspace=None):
+    """Prefill. q [B,H_q,S_q,d], k/v [B,H_kv,S_k,d] (bf16, CUDA) -> out [B,H_q,S_q,d].
+
+    workspace: None -- when the library would rotate the keys once before the
+    prefill (fwd_workspace_bytes > 0), a buffer for them is taken from torch's
+    allocator and apex_attn_fwd_ws runs; a uint8 CUDA tensor -- that buffer;
+    False -- no workspace (apex_attn_fwd / apex_attn_fwd_ex)."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check(t, n, 4)
@@ -200,8 +230,21 @@ def fwd(q, k, v, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.0
     if out is None:
         out = torch.empty_like(q)
     _check(out, "out", 4)
+    if workspace is None:
+        need = fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d, window=window, q_pos0=q_pos0, rope_base=rope_base,
+                                   yarn_scale=yarn_scale, yarn_beta_fast=yarn_beta_fast,
+                                   yarn_beta_slow=yarn_beta_slow, prefix_len=prefix_len,
+                                   keys_prerotated=keys_prerotated)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     plain = yarn_scale <= 1.0 and prefix_len == 0 and not keys_prerotated
-    if plain:
+    if workspace is not None and workspace is not False:
+        opt = _options(window, q_pos0, rope_base, yarn_scale, yarn_beta_fast, yarn_beta_slow, prefix_len,
+                       keys_prerotated)
+        st = apex_attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H_q, H_kv, S_q, S_k,
+                              d, opt, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                              _stream_handle(stream))
+    elif plain:
         st = apex_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H_q, H_kv, S_q, S_k, d,
                            int(window), int(q_pos0), float(rope_base), _stream_handle(stream))
     else:

@@ -275,6 +275,38 @@ SplitPlan plan_decode(int units, int n_stages, int capacity)
 
 int max_stages_for(int S_k) { return (S_k + kDecodeKeysPerStage - 1) / kDecodeKeysPerStage + 1; }
 
+// --- keys rotated once before the prefill.  Every work item of the prefill
+// rotates the key tiles it visits (in shared memory); a key tile is visited
+// by every item whose window reaches it, so it is rotated up to S / W times
+// (about 9 on B4 H_q32 S4096 W1024, 33 on S65536 W4096, 130 on a G = 16
+// causal S8192).  Rotating the keys once into a workspace costs a read and a
+// write of K.  Measured on GB300: about 1.7 ns of kernel time per (item, key
+// tile) visit, against 10 ns per 128-key tile for the pass and about 1 us for
+// its launch (the prefill, a programmatic dependent, sets up during the pass);
+// the pass is used when it costs less than the visits it saves.
+struct PrerotatePlan {
+    bool use;
+    int n_pos;  // keys rotated (whole 128-key tiles up to the last one any item reads)
+};
+
+PrerotatePlan plan_prerotate(int units, int S_q, int S_k, int q_pos0, int window, int P, int block_rows)
+{
+    long long visits = 0;
+    int kmax = 0;
+    for (int r0 = 0; r0 < S_q; r0 += block_rows) {
+        const int rows = std::min(block_rows, S_q - r0);
+        const int m_first = q_pos0 + r0, m_last = q_pos0 + r0 + rows - 1;
+        const int key_lo = (m_first < P || window <= 0) ? 0 : std::max(0, m_first - window + 1);
+        const int key_hi = (m_first < P) ? std::max(m_last, P - 1) : m_last;
+        visits += key_hi / 128 - key_lo / 128 + 1;
+        kmax = std::max(kmax, key_hi);
+    }
+    const int n_pos = std::min(S_k, (kmax / 128 + 1) * 128);
+    const long long tiles = (long long)units * ((n_pos + 127) / 128);
+    visits *= units;
+    return PrerotatePlan{visits * 17 >= tiles * 100 + 10000, n_pos};
+}
+
 }  // namespace
 }  // namespace apex
 
@@ -475,7 +507,7 @@ apex_status apex_attn_decode(const void *q, const void *k_cache, const void *v_c
 // attention (d_qk = d_v + d_rope): validation done by the callers.
 apex_status prefill_launch(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv, int S_q,
                            int S_k, int d_qk, int d_v, int d_rope, const apex_attn_options *opt, const RopeFreq &f,
-                           apex_stream_t stream)
+                           apex_stream_t stream, void *workspace = nullptr)
 {
     const int q_pos0 = opt->q_pos, window = opt->window, P = opt->prefix_len;
     if (S_q <= 0 || q_pos0 < 0 || (long long)q_pos0 + S_q > (long long)S_k) return APEX_ERR_INVALID_ARG;
@@ -496,10 +528,33 @@ apex_status prefill_launch(const void *q, const void *k, const void *v, void *ou
     const int G = H_q / H_kv;
     const int rows_per_head = 128 / G;
     const bool pair = mla || use_pair_prefill(d_qk, st->sm_count);
+    // keys rotated once into the workspace (plain block on CTA pairs) when that
+    // costs less than rotating them in every work item that visits them
+    const void *keys = k;
+    bool prerotated = opt->keys_prerotated != 0;
+    if (workspace && pair && !mla && !prerotated) {
+        const PrerotatePlan pr = plan_prerotate(B * H_kv, S_q, S_k, q_pos0, window > 0 ? window : 0, P,
+                                                4 * rows_per_head);
+        if (pr.use) {
+            RopeKeysParams rp;
+            rp.in = static_cast<const uint16_t *>(k);
+            rp.out = static_cast<uint16_t *>(workspace);
+            rp.in_stride = rp.out_stride = (long long)S_k * d_qk;
+            rp.n_heads = B * H_kv;
+            rp.n_pos = pr.n_pos;
+            rp.d_h = d_qk;
+            rp.pos0 = 0;
+            rp.rope = tv;
+            if (launch_rope_keys(rp, st->sm_count, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+                return APEX_ERR_CUDA;
+            keys = workspace;
+            prerotated = true;
+        }
+    }
     PrefillLaunch L;
     memset(&L, 0, sizeof L);
     if (!make_map(&L.tm_q, q, d_qk, S_q, B * H_q, rows_per_head, G) ||
-        !make_map(&L.tm_k, k, d_qk, S_k, B * H_kv, pair ? 64 : 128, 1) ||
+        !make_map(&L.tm_k, keys, d_qk, S_k, B * H_kv, pair ? 64 : 128, 1) ||
         !make_map(&L.tm_v, v, d_v, S_k, B * H_kv, 128, 1))
         return APEX_ERR_CUDA;
     if (pair && (d_v != 128 || !make_out_map(&L.tm_o, out, S_q, G, B * H_kv))) return APEX_ERR_CUDA;
@@ -518,7 +573,7 @@ apex_status prefill_launch(const void *q, const void *k, const void *v, void *ou
     p.window = window > 0 ? window : 0;
     p.q_pos0 = q_pos0;
     p.prefix_len = P;
-    p.keys_prerotated = opt->keys_prerotated != 0;
+    p.keys_prerotated = prerotated;
     p.rows_per_head = rows_per_head;
     const int block_rows = (pair ? 4 : 2) * rows_per_head;
     p.n_qblocks = (S_q + block_rows - 1) / block_rows;
@@ -544,6 +599,36 @@ apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *
     apex_status s = check_common(B, H_q, H_kv, S_k, d_h, f.base);
     if (s != APEX_OK) return s;
     return prefill_launch(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, d_h, d_h, opt, f, stream);
+}
+
+size_t apex_attn_fwd_workspace_bytes(int B, int H_q, int H_kv, int S_q, int S_k, int d_h,
+                                     const apex_attn_options *opt)
+{
+    if (!opt || opt->keys_prerotated) return 0;
+    RopeFreq f;
+    if (!freq_of(*opt, &f) || check_common(B, H_q, H_kv, S_k, d_h, f.base) != APEX_OK) return 0;
+    const int q_pos0 = opt->q_pos, P = opt->prefix_len;
+    if (S_q <= 0 || q_pos0 < 0 || (long long)q_pos0 + S_q > (long long)S_k || P < 0 || P > S_k) return 0;
+    if (!use_pair_prefill(d_h, 2)) return 0;  // the pass serves the CTA-pair kernel only
+    const PrerotatePlan pr = plan_prerotate(B * H_kv, S_q, S_k, q_pos0, opt->window > 0 ? opt->window : 0, P,
+                                            4 * (128 / (H_q / H_kv)));
+    return pr.use ? (size_t)B * H_kv * (size_t)S_k * d_h * 2 : 0;
+}
+
+apex_status apex_attn_fwd_ws(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
+                             int S_q, int S_k, int d_h, const apex_attn_options *opt, void *workspace,
+                             size_t workspace_bytes, apex_stream_t stream)
+{
+    if (!q || !k || !v || !out || !opt) return APEX_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return APEX_ERR_INVALID_ARG;
+    RopeFreq f;
+    if (!freq_of(*opt, &f)) return APEX_ERR_INVALID_ARG;
+    apex_status s = check_common(B, H_q, H_kv, S_k, d_h, f.base);
+    if (s != APEX_OK) return s;
+    if (workspace &&
+        (!aligned16(workspace) || workspace_bytes < apex_attn_fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h, opt)))
+        return APEX_ERR_INVALID_ARG;
+    return prefill_launch(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, d_h, d_h, opt, f, stream, workspace);
 }
 
 apex_status apex_attn_mla_fwd(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,

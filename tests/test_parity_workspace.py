@@ -101,3 +101,37 @@ def test_prerotated_keys_never_use_the_workspace():
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
     assert bool((ws.view(torch.int16) == NAN_BF16).all())
+
+
+def test_pass_and_prefill_captured_in_a_graph():
+    """The two kernels of a prefill that rotates its keys beforehand (the pass,
+    and the prefill launched as its programmatic dependent) captured in one CUDA
+    graph, replayed on new inputs copied into the same buffers."""
+    dev = _dev()
+    B, H_q, H_kv, S, d, W = 2, 8, 2, 8192, 128, 4096
+    assert apex.fwd_workspace_bytes(B, H_q, H_kv, S, S, d, window=W) > 0
+    q, k, v = (t.to(dev) for t in inputs.make_qkv(B, H_q, H_kv, S, S, d, 8100))
+    out = torch.empty_like(q)
+    ws = _ws(B, H_kv, S, d, dev)
+    apex.fwd(q, k, v, window=W, out=out, workspace=ws)  # table built, module loaded
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            apex.fwd(q, k, v, window=W, out=out, workspace=ws, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    rows = _rows(S, 11)
+    for seed in (8101, 8102):
+        qh, kh, vh = inputs.make_qkv(B, H_q, H_kv, S, S, d, seed)
+        q.copy_(qh)
+        k.copy_(kh)
+        v.copy_(vh)
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.attn(qh, kh, vh, window=W, rows=rows)
+        mx, mean = _errs(out[:, :, rows].cpu(), ref)
+        assert mx <= MAX_ERR and mean <= MEAN_ERR, (seed, mx, mean)
+    assert apex.apex_attn_device_status() == 0

@@ -1,8 +1,11 @@
 """Benchmark of the APEX-1 attention hot path on GB300.
 
 One step = one pass of the whole hot path on synthetic, seeded bf16 inputs:
-  * apex_attn_fwd on the GQA prefill workload (B=4, H_q=32, H_kv=8, S=4096,
-    d_h=128, causal + window 1024): RoPE, QK^T, mask/skip, online softmax, PV;
+  * the prefill call on the GQA prefill workload (B=4, H_q=32, H_kv=8, S=4096,
+    d_h=128, causal + window 1024): RoPE, QK^T, mask/skip, online softmax, PV --
+    through apex.fwd, i.e. apex_attn_fwd_ws with a workspace from torch, which
+    on this workload rotates the keys once (rope_keys kernel) before the
+    prefill kernel; the call's time covers both;
   * apex_attn_decode on the decode workload (B=64, H_q=32, H_kv=8, one query at
     position 32767 against a 32768-entry bf16 KV cache, d_h=128): split-KV
     kernel + log-sum-exp combine.

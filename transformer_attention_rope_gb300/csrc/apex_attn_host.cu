@@ -277,7 +277,7 @@ int max_stages_for(int S_k) { return (S_k + kDecodeKeysPerStage - 1) / kDecodeKe
 
 // --- keys rotated once before the prefill.  Every work item of the prefill
 // rotates the key tiles it visits (in shared memory); a key tile is visited
-// by every item whose window reaches it, so it is rotated up to S / W times
+// by every item whose key range covers it, so it is rotated that many times
 // (about 9 on B4 H_q32 S4096 W1024, 33 on S65536 W4096, 130 on a G = 16
 // causal S8192).  Rotating the keys once into a workspace costs a read and a
 // write of K.  Measured on GB300: about 1.7 ns of kernel time per (item, key
@@ -530,34 +530,29 @@ apex_status prefill_launch(const void *q, const void *k, const void *v, void *ou
     const bool pair = mla || use_pair_prefill(d_qk, st->sm_count);
     // keys rotated once into the workspace (plain block on CTA pairs) when that
     // costs less than rotating them in every work item that visits them
-    const void *keys = k;
-    bool prerotated = opt->keys_prerotated != 0;
-    if (workspace && pair && !mla && !prerotated) {
-        const PrerotatePlan pr = plan_prerotate(B * H_kv, S_q, S_k, q_pos0, window > 0 ? window : 0, P,
-                                                4 * rows_per_head);
-        if (pr.use) {
-            RopeKeysParams rp;
-            rp.in = static_cast<const uint16_t *>(k);
-            rp.out = static_cast<uint16_t *>(workspace);
-            rp.in_stride = rp.out_stride = (long long)S_k * d_qk;
-            rp.n_heads = B * H_kv;
-            rp.n_pos = pr.n_pos;
-            rp.d_h = d_qk;
-            rp.pos0 = 0;
-            rp.rope = tv;
-            if (launch_rope_keys(rp, st->sm_count, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-                return APEX_ERR_CUDA;
-            keys = workspace;
-            prerotated = true;
-        }
-    }
+    PrerotatePlan pre{false, 0};
+    if (workspace && pair && !mla && !opt->keys_prerotated)
+        pre = plan_prerotate(B * H_kv, S_q, S_k, q_pos0, window > 0 ? window : 0, P, 4 * rows_per_head);
     PrefillLaunch L;
     memset(&L, 0, sizeof L);
     if (!make_map(&L.tm_q, q, d_qk, S_q, B * H_q, rows_per_head, G) ||
-        !make_map(&L.tm_k, keys, d_qk, S_k, B * H_kv, pair ? 64 : 128, 1) ||
+        !make_map(&L.tm_k, pre.use ? workspace : k, d_qk, S_k, B * H_kv, pair ? 64 : 128, 1) ||
         !make_map(&L.tm_v, v, d_v, S_k, B * H_kv, 128, 1))
         return APEX_ERR_CUDA;
     if (pair && (d_v != 128 || !make_out_map(&L.tm_o, out, S_q, G, B * H_kv))) return APEX_ERR_CUDA;
+    if (pre.use) {
+        RopeKeysParams rp;
+        rp.in = static_cast<const uint16_t *>(k);
+        rp.out = static_cast<uint16_t *>(workspace);
+        rp.in_stride = rp.out_stride = (long long)S_k * d_qk;
+        rp.n_heads = B * H_kv;
+        rp.n_pos = pre.n_pos;
+        rp.d_h = d_qk;
+        rp.pos0 = 0;
+        rp.rope = tv;
+        if (launch_rope_keys(rp, st->sm_count, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return APEX_ERR_CUDA;
+    }
     PrefillParams &p = L.p;
     p.out = static_cast<uint16_t *>(out);
     p.rope = tv;
@@ -573,7 +568,7 @@ apex_status prefill_launch(const void *q, const void *k, const void *v, void *ou
     p.window = window > 0 ? window : 0;
     p.q_pos0 = q_pos0;
     p.prefix_len = P;
-    p.keys_prerotated = prerotated;
+    p.keys_prerotated = pre.use || opt->keys_prerotated != 0;
     p.rows_per_head = rows_per_head;
     const int block_rows = (pair ? 4 : 2) * rows_per_head;
     p.n_qblocks = (S_q + block_rows - 1) / block_rows;

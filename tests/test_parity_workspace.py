@@ -135,3 +135,31 @@ def test_pass_and_prefill_captured_in_a_graph():
         mx, mean = _errs(out[:, :, rows].cpu(), ref)
         assert mx <= MAX_ERR and mean <= MEAN_ERR, (seed, mx, mean)
     assert apex.apex_attn_device_status() == 0
+
+
+@pytest.mark.parametrize("H_q,H_kv,window", [(32, 2, 0), (8, 2, 2500)])
+def test_pass_on_a_chunk_of_a_longer_sequence(H_q, H_kv, window):
+    """A prefill of rows at positions 3000..6999 against 9001 keys (the last
+    2001 never visible): the pass rotates the keys up to the end of the last
+    128-key tile any work item reads and leaves the rest of the workspace as
+    it was; the output matches the oracle."""
+    dev = _dev()
+    B, S_q, S_k, q_pos0, d = 1, 4000, 9001, 3000, 128
+    assert apex.fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d, window=window, q_pos0=q_pos0) > 0
+    q = inputs.normal_bf16((B, H_q, S_q, d), 8300 + H_q, 0)
+    k = inputs.normal_bf16((B, H_kv, S_k, d), 8300 + H_q, 1)
+    v = inputs.normal_bf16((B, H_kv, S_k, d), 8300 + H_q, 2)
+    kd = k.to(dev)
+    ws = _ws(B, H_kv, S_k, d, dev)
+    out = apex.fwd(q.to(dev), kd, v.to(dev), window=window, q_pos0=q_pos0, workspace=ws)
+    torch.cuda.synchronize()
+    n_pos = ((q_pos0 + S_q - 1) // 128 + 1) * 128  # 7040
+    held = ws.view(torch.int16).view(B, H_kv, S_k, d)
+    rot = apex.rope_keys(kd).view(torch.int16)
+    assert torch.equal(held[:, :, :n_pos], rot[:, :, :n_pos])
+    assert bool((held[:, :, n_pos:] == NAN_BF16).all())
+    rows = _rows(S_q, 9)
+    ref = oracle.attn(q, k, v, window=window, q_pos0=q_pos0, rows=rows)
+    mx, mean = _errs(out[:, :, rows].cpu(), ref)
+    assert mx <= MAX_ERR and mean <= MEAN_ERR, (mx, mean)
+    assert apex.apex_attn_device_status() == 0

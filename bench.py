@@ -610,15 +610,15 @@ def prefill_call(apex, w, q, k, v, out, feat):
 def prefill_kernel_name(w, feat=None):
     """The prefill kernel a call runs, and whether the keys are rotated once by
     rope_keys_kernel before it (the call's time covers both)."""
-    if not w.d_r and (w.d_h != 128 or os.environ.get("APEX_ATTN_PREFILL") == "single"):
-        return "prefill_kernel", False
     if w.d_r:
         return "prefill_pair_kernel", False
     import transformer_attention_rope_gb300 as apex
+    name = ("prefill_kernel" if (w.d_h != 128 or os.environ.get("APEX_ATTN_PREFILL") == "single")
+            else "prefill_pair_kernel")
     opts = {k: v for k, v in (feat or {}).items()}
     prerot = apex.fwd_workspace_bytes(w.B, w.H_q, w.H_kv, w.S_q, w.S_k, w.d_h, window=w.window, q_pos0=w.q_pos0,
                                       rope_base=w.rope_base, **opts) > 0
-    return "prefill_pair_kernel", prerot
+    return name, prerot
 
 
 def call_traffic(traffic, key, prerot):

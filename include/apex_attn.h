@@ -145,7 +145,7 @@ size_t apex_attn_fwd_workspace_bytes(int B, int H_q, int H_kv, int S_q, int S_k,
  *     or out, not read before written; a smaller or misaligned workspace gives
  *     APEX_ERR_INVALID_ARG before any launch.
  *   The pass is a second kernel on `stream` before the prefill; with
- *   opt->keys_prerotated, or on the single-CTA kernel (d_h = 64), no pass runs.
+ *   opt->keys_prerotated no pass runs.
  * Errors as for apex_attn_fwd_ex.
  */
 apex_status apex_attn_fwd_ws(const void *q, const void *k, const void *v, void *out,

@@ -141,10 +141,12 @@ def test_fwd_workspace_bytes(lib):
                           ((1, 32, 8, 65536, 65536, 128), 4096)):
         B, H_q, H_kv, S_q, S_k, d = shape
         assert apex.fwd_workspace_bytes(*shape, window=window) == B * H_kv * S_k * d * 2
-    # ... none for small problems, pre-rotated keys, d_h = 64 (single-CTA kernel) or bad sizes
+    # ... also on the single-CTA kernel (d_h = 64), ...
+    assert apex.fwd_workspace_bytes(1, 128, 8, 8192, 8192, 64) == 8 * 8192 * 64 * 2
+    # ... none for small problems, pre-rotated keys or bad sizes
     assert apex.fwd_workspace_bytes(1, 4, 2, 256, 256, 128) == 0
+    assert apex.fwd_workspace_bytes(1, 4, 2, 128, 128, 64) == 0          # the tiny workload
     assert apex.fwd_workspace_bytes(4, 32, 8, 4096, 4096, 128, window=1024, keys_prerotated=True) == 0
-    assert apex.fwd_workspace_bytes(4, 32, 8, 4096, 4096, 64, window=1024) == 0
     assert apex.fwd_workspace_bytes(1, 3, 2, 4096, 4096, 128) == 0
     assert apex.fwd_workspace_bytes(1, 4, 2, 4096, 4000, 128) == 0   # S_q > S_k
     assert apex.apex_attn_fwd_workspace_bytes(4, 32, 8, 4096, 4096, 128, None) == 0

@@ -42,15 +42,16 @@ def _rows(S, step):
 
 
 # shapes on which each key tile is visited often enough for the pass to run
-@pytest.mark.parametrize("B,H_q,H_kv,S,window,opts", [
-    (2, 8, 2, 8192, 4096, {}),                                   # G = 4, sliding window
-    (1, 32, 2, 8192, 0, {}),                                     # G = 16, causal
-    (2, 8, 2, 8192, 4096, dict(yarn_scale=8.0)),                 # YaRN frequencies in the pass
-    (1, 16, 4, 6000, 0, dict(prefix_len=700)),                   # prefix, ragged last tile
+@pytest.mark.parametrize("B,H_q,H_kv,S,window,opts,d", [
+    (2, 8, 2, 8192, 4096, {}, 128),                              # G = 4, sliding window
+    (1, 32, 2, 8192, 0, {}, 128),                                # G = 16, causal
+    (2, 8, 2, 8192, 4096, dict(yarn_scale=8.0), 128),            # YaRN frequencies in the pass
+    (1, 16, 4, 6000, 0, dict(prefix_len=700), 128),              # prefix, ragged last tile
+    (2, 8, 2, 8192, 4096, {}, 64),                               # d_h = 64: the single-CTA kernel
+    (1, 32, 2, 6000, 0, {}, 64),                                 # d_h = 64, G = 16, ragged
 ])
-def test_pass_runs_and_matches_oracle(B, H_q, H_kv, S, window, opts):
+def test_pass_runs_and_matches_oracle(B, H_q, H_kv, S, window, opts, d):
     dev = _dev()
-    d = 128
     q, k, v = inputs.make_qkv(B, H_q, H_kv, S, S, d, 7700 + S + H_q)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     assert apex.fwd_workspace_bytes(B, H_q, H_kv, S, S, d, window=window, **opts) == B * H_kv * S * d * 2

@@ -531,8 +531,8 @@ apex_status prefill_launch(const void *q, const void *k, const void *v, void *ou
     // keys rotated once into the workspace (plain block on CTA pairs) when that
     // costs less than rotating them in every work item that visits them
     PrerotatePlan pre{false, 0};
-    if (workspace && pair && !mla && !opt->keys_prerotated)
-        pre = plan_prerotate(B * H_kv, S_q, S_k, q_pos0, window > 0 ? window : 0, P, 4 * rows_per_head);
+    if (workspace && !mla && !opt->keys_prerotated)
+        pre = plan_prerotate(B * H_kv, S_q, S_k, q_pos0, window > 0 ? window : 0, P, (pair ? 4 : 2) * rows_per_head);
     PrefillLaunch L;
     memset(&L, 0, sizeof L);
     if (!make_map(&L.tm_q, q, d_qk, S_q, B * H_q, rows_per_head, G) ||
@@ -604,9 +604,10 @@ size_t apex_attn_fwd_workspace_bytes(int B, int H_q, int H_kv, int S_q, int S_k,
     if (!freq_of(*opt, &f) || check_common(B, H_q, H_kv, S_k, d_h, f.base) != APEX_OK) return 0;
     const int q_pos0 = opt->q_pos, P = opt->prefix_len;
     if (S_q <= 0 || q_pos0 < 0 || (long long)q_pos0 + S_q > (long long)S_k || P < 0 || P > S_k) return 0;
-    if (!use_pair_prefill(d_h, 2)) return 0;  // the pass serves the CTA-pair kernel only
+    // a work item covers 4 M tiles of 128 / G query rows on CTA pairs, 2 on one CTA
+    const int block_rows = (use_pair_prefill(d_h, 2) ? 4 : 2) * (128 / (H_q / H_kv));
     const PrerotatePlan pr = plan_prerotate(B * H_kv, S_q, S_k, q_pos0, opt->window > 0 ? opt->window : 0, P,
-                                            4 * (128 / (H_q / H_kv)));
+                                            block_rows);
     return pr.use ? (size_t)B * H_kv * (size_t)S_k * d_h * 2 : 0;
 }
 

@@ -98,3 +98,23 @@ def test_decode_writes_only_its_output_and_workspace(mla):
         apex.decode(q, k, v, S_k - 1, window=700, out=out, workspace=ws_u8)
     assert _guards_intact(obuf) and _guards_intact(wbuf)
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("kernel,d,B,H_q,H_kv,S,window", [
+    ("pair", 128, 1, 32, 2, 6000, 0),
+    ("single", 64, 2, 8, 2, 8192, 4096),
+])
+def test_prefill_with_key_pass_writes_only_its_output_and_workspace(monkeypatch, kernel, d, B, H_q, H_kv, S,
+                                                                    window):
+    """The key-rotation pass writes only inside the workspace, the prefill only
+    inside its output (shapes on which the library's cost model runs the pass)."""
+    dev = _dev()
+    monkeypatch.setenv("APEX_ATTN_PREFILL", kernel)
+    nbytes = apex.fwd_workspace_bytes(B, H_q, H_kv, S, S, d, window=window)
+    assert nbytes == B * H_kv * S * d * 2
+    q, k, v = [t.to(dev) for t in inputs.make_qkv(B, H_q, H_kv, S, S, d, 3200 + S)]
+    obuf, out = _guarded((B, H_q, S, d), dev)
+    wbuf, ws = _guarded((nbytes // 2,), dev)
+    apex.fwd(q, k, v, window=window, out=out, workspace=ws.view(torch.uint8))
+    assert _guards_intact(obuf) and _guards_intact(wbuf)
+    assert torch.isfinite(out.float()).all()

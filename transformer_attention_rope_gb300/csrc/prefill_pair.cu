@@ -23,8 +23,10 @@
 //
 // Warps per CTA: 0-3 / 4-7 softmax + epilogue of tiles 0 / 1 (and their Q
 // RoPE), 8-11 K RoPE (their "K ready" arrival also vouches that the V tile of
-// the same index has landed, so the MMA thread has one wait less per tile),
-// 12 TMA producer, 13 MMA issuer (leader) / TMEM allocation, 14-15 idle.
+// the same index has landed, so the MMA thread has one wait less per tile; in
+// the instance for keys rotated beforehand they turn no K tile, and for G >= 8
+// rotate a share of the Q tiles instead), 12 TMA producer, 13 MMA issuer
+// (leader) / TMEM allocation, 14-15 idle.
 #include <math.h>
 
 #include "device_common.cuh"
@@ -295,6 +297,46 @@ __device__ __forceinline__ void rope_q_tile(uint8_t *tile, int rt, const float2 
     }
 }
 
+// Part of a Q tile: combos q = q_first, q_first + q_step, ... (< 8P) of position
+// q >> 3 and chunk q & 7, heads [h_lo, h_hi) of each.
+template <int NRB, int B0>
+__device__ __forceinline__ void rope_q_part(uint8_t *tile, const float2 *table, int pos0, int P, int valid_p,
+                                            int q_first, int q_step, int h_lo, int h_hi)
+{
+    constexpr int kHalf = 32 * NRB;
+    for (int q = q_first; q < P * 8; q += q_step) {
+        const int pp = q >> 3, c = q & 7;
+        if (pp >= valid_p) continue;
+        uint64_t C[NRB][2], S[NRB][2];
+#pragma unroll
+        for (int bx = 0; bx < NRB; ++bx) {
+            const float4 *t = reinterpret_cast<const float4 *>(table + (size_t)(pos0 + pp) * kHalf + 32 * bx + 4 * c);
+            const float4 a = __ldg(t), b = __ldg(t + 1);
+            C[bx][0] = f2_pack(a.x, a.z);
+            S[bx][0] = f2_pack(a.y, a.w);
+            C[bx][1] = f2_pack(b.x, b.z);
+            S[bx][1] = f2_pack(b.y, b.w);
+        }
+        for (int hl = h_lo; hl < h_hi; ++hl) {
+            const int row = hl * P + pp;
+#pragma unroll
+            for (int bx = 0; bx < NRB; ++bx) {
+                uint4 *ptr = reinterpret_cast<uint4 *>(tile + (B0 + bx) * kQBox + swz128(row, c));
+                *ptr = rope_chunk(*ptr, C[bx], S[bx]);
+            }
+        }
+    }
+}
+
+// With the keys rotated beforehand (the K-RoPE warps have no K tiles to turn)
+// and G >= 8, the K-RoPE warps rotate the last G / 4 heads of both Q tiles of
+// each item, the softmax warps the others: per thread 6 (position, head) pairs
+// instead of 8 (G = 8) or 16 (G = 16, where only 64 positions x 8 chunks exist
+// for 128 threads).  Measured: G = 16 3.5 % faster; at G = 4, where the softmax
+// warps' share only drops from 8 to 6, it is not faster.
+__device__ __forceinline__ bool q_shared(bool krot, int G) { return !krot && G >= 8; }
+__device__ __forceinline__ int q_heads_softmax(int G) { return G - G / 4; }
+
 // ---------------------------------------------------------------- work items
 // One item: a (batch, kv head) unit and a block of 4P query rows (P = 128 / G):
 // tile T = 2 rank + t of the pair covers rows r0 + T P .. r0 + T P + P - 1.
@@ -328,7 +370,9 @@ __device__ __forceinline__ int item_index(int k)
     return k * g + ((k & 1) ? (g - 1 - c) : c);
 }
 
-template <int DQK, int DR>
+// KROT: the K tiles are rotated in shared memory (unless p.keys_prerotated);
+// false: the instance for keys the library rotated once beforehand.
+template <int DQK, int DR, bool KROT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -356,7 +400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         *abort = 0u;
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(kBarQFull + t), 1);
-            mbar_init(bar(kBarQReady + t), 8);
+            mbar_init(bar(kBarQReady + t), q_shared(KROT, p.G) ? 16 : 8);
             mbar_init(bar(kBarQEmpty + t), 1);
             mbar_init(bar(kBarSFull + t), 1);
             mbar_init(bar(kBarPReady + t), 8);
@@ -507,16 +551,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int max_row = p.rope.max_pos - 1;
         const int half0 = 64 * (int)rank;
         KHalfRope<C::kRopeBoxes, C::kRopeBox0> kr;
-        kr.init(p.rope.cs, c);
+        if (KROT) kr.init(p.rope.cs, c);
         int kc = 0;
         for (int k = 0, w = item_index(0); w < p.n_work; ++k, w = item_index(k)) {
             const Item it = make_item(p, w);
-            kr.load_seed(p.rope.cs, min(128 * it.j_lo + half0 + r0, max_row), c);
+            if (q_shared(KROT, p.G)) {
+                // this CTA's share of the item's Q tiles: heads [hs, G) of both
+                const int hs = q_heads_softmax(p.G);
+                for (int t = 0; t < 2; ++t) {
+                    const int T = 2 * (int)rank + t;
+                    pair_wait(bar(kBarQFull + t), k & 1, p.wait, abort);
+                    const bool mine = p.G < 16 || (rt >> 6) == t;  // G = 16: threads 64 t .. 64 t + 63
+                    if (mine)
+                        rope_q_part<C::kRopeBoxes, C::kRopeBox0>(
+                            smem + kQOff + t * kQTile, p.rope.cs, p.q_pos0 + it.r0 + T * P, P,
+                            min(P, p.S_q - (it.r0 + T * P)), p.G < 16 ? rt : (rt & 63), p.G < 16 ? 128 : 64, hs, p.G);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) arrive_leader(bar(kBarQReady + t));
+                }
+            }
+            if (KROT) kr.load_seed(p.rope.cs, min(128 * it.j_lo + half0 + r0, max_row), c);
             for (int j = 0; j < it.n_kt; ++j, ++kc) {
                 const int ks = kc % kKStages;
                 pair_wait(bar(kBarKFull + ks), (kc / kKStages) & 1, p.wait, abort);
-                if (!p.keys_prerotated) kr.rotate(smem + kKOff + ks * kKTile, rt);
-                if (j + 1 < it.n_kt) kr.load_seed(p.rope.cs, min(128 * (it.j_lo + j + 1) + half0 + r0, max_row), c);
+                if (KROT && !p.keys_prerotated) kr.rotate(smem + kKOff + ks * kKTile, rt);
+                if (KROT && j + 1 < it.n_kt)
+                    kr.load_seed(p.rope.cs, min(128 * (it.j_lo + j + 1) + half0 + r0, max_row), c);
                 // K(j) ready also means V(j) has landed: the MMA thread waits for
                 // KReady(j) before QK(j), which precedes PV(j)
                 pair_wait(bar(kBarVFull + kc % kVStages), (kc / kVStages) & 1, p.wait, abort);
@@ -537,9 +598,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t o_addr = lane_base + col_o(t);
         auto rotate_q = [&](const Item &it, int k) {
             pair_wait(bar(kBarQFull + t), k & 1, p.wait, abort);
-            rope_q_tile<C::kRopeBoxes, C::kRopeBox0>(smem + kQOff + t * kQTile, i, p.rope.cs,
-                                                     p.q_pos0 + it.r0 + T * P, p.G, P,
-                                                     min(P, p.S_q - (it.r0 + T * P)));
+            if (q_shared(KROT, p.G)) {
+                const int hs = q_heads_softmax(p.G);
+                if (p.G < 16)
+                    rope_q_part<C::kRopeBoxes, C::kRopeBox0>(smem + kQOff + t * kQTile, p.rope.cs,
+                                                             p.q_pos0 + it.r0 + T * P, P,
+                                                             min(P, p.S_q - (it.r0 + T * P)), i, 128, 0, hs);
+                else  // G = 16: two threads per combo, 6 heads each
+                    rope_q_part<C::kRopeBoxes, C::kRopeBox0>(smem + kQOff + t * kQTile, p.rope.cs,
+                                                             p.q_pos0 + it.r0 + T * P, P,
+                                                             min(P, p.S_q - (it.r0 + T * P)), i >> 1, 128,
+                                                             6 * (i & 1), 6 * (i & 1) + 6);
+            } else {
+                rope_q_tile<C::kRopeBoxes, C::kRopeBox0>(smem + kQOff + t * kQTile, i, p.rope.cs,
+                                                         p.q_pos0 + it.r0 + T * P, p.G, P,
+                                                         min(P, p.S_q - (it.r0 + T * P)));
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) arrive_leader(bar(kBarQReady + t));
@@ -708,20 +782,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int DQK, int DR>
+template <int DQK, int DR, bool KROT>
 cudaError_t launch_pair_t(const PrefillLaunch &L, cudaStream_t stream)
 {
     using C = PairCfg<DQK, DR>;
-    cudaError_t err = cudaFuncSetAttribute(prefill_pair_kernel<DQK, DR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(prefill_pair_kernel<DQK, DR, KROT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            C::kSmemBytes);
     if (err != cudaSuccess) return err;
     // setmaxnreg.inc blocks until the block's own pool can serve it: never
     // launch unless the split fits the registers the block is launched with
     cudaFuncAttributes fa;
-    err = cudaFuncGetAttributes(&fa, prefill_pair_kernel<DQK, DR>);
+    err = cudaFuncGetAttributes(&fa, prefill_pair_kernel<DQK, DR, KROT>);
     if (err != cudaSuccess) return err;
     if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-    return launch_dependent(prefill_pair_kernel<DQK, DR>, L.grid, kThreads, C::kSmemBytes, stream, L.tm_q, L.tm_k,
+    return launch_dependent(prefill_pair_kernel<DQK, DR, KROT>, L.grid, kThreads, C::kSmemBytes, stream, L.tm_q, L.tm_k,
                             L.tm_v, L.tm_o, L.p);
 }
 
@@ -730,8 +804,9 @@ cudaError_t launch_pair_t(const PrefillLaunch &L, cudaStream_t stream)
 cudaError_t launch_prefill_pair(const PrefillLaunch &L, cudaStream_t stream)
 {
     if (L.grid & 1) return cudaErrorInvalidValue;
-    if (L.p.d_h == 128 && L.p.d_rope == 128) return launch_pair_t<128, 128>(L, stream);
-    if (L.p.d_h == 192 && L.p.d_rope == 64) return launch_pair_t<192, 64>(L, stream);
+    if (L.p.d_h == 128 && L.p.d_rope == 128)
+        return L.p.keys_prerotated ? launch_pair_t<128, 128, false>(L, stream) : launch_pair_t<128, 128, true>(L, stream);
+    if (L.p.d_h == 192 && L.p.d_rope == 64) return launch_pair_t<192, 64, true>(L, stream);
     return cudaErrorInvalidValue;
 }
 

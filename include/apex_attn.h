@@ -21,9 +21,11 @@
  * - Tensors are dense, row-major, bf16 (raw 16-bit patterns), in device
  *   memory, with the 4-D attention layout [B, H, S, d_h] (Part 1 §1 "Tensor
  *   Shape Convention").  Every pointer must be 16-byte aligned.
- * - The caller owns every buffer it passes.  The library owns only a per-device
- *   cache of RoPE cos/sin tables (fp32, built in double precision on the host),
- *   allocated on first use and grown on demand.  A call that has to build or
+ * - The caller owns every buffer it passes, scratch included: the decode's
+ *   split partials and the prefill's rotated keys live in workspaces the caller
+ *   passes (sizes from the *_workspace_bytes functions).  The library owns only
+ *   a per-device cache of RoPE cos/sin tables (fp32, built in double precision
+ *   on the host), allocated on first use and grown on demand.  A call that has to build or
  *   grow that table allocates device memory and synchronises the device;
  *   apex_attn_rope_reserve() builds it ahead of time.
  * - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default

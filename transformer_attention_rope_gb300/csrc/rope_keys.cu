@@ -18,6 +18,9 @@ __global__ void __launch_bounds__(256) rope_keys_kernel(const RopeKeysParams p)
 {
     constexpr int kChunks = 1 << LOG2C;
     constexpr int kHalf = 4 * kChunks;
+    // launched as a programmatic dependent: the keys may be the previous
+    // kernel's output, so nothing is read before that kernel is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int per_head = p.n_pos * kChunks;
     const int h_groups = (p.n_heads + kHeads - 1) / kHeads;
     for (int hg = blockIdx.y; hg < h_groups; hg += gridDim.y) {
@@ -56,11 +59,21 @@ cudaError_t launch_rope_keys(const RopeKeysParams &p, int sm_count, cudaStream_t
     int gx = (per_head + 255) / 256;
     const int gx_want = (target + gy - 1) / gy;
     if (gx > gx_want) gx = gx_want;
-    const dim3 grid(gx > 0 ? gx : 1, gy > 0 ? gy : 1);
-    if (p.d_h == 128) rope_keys_kernel<4><<<grid, 256, 0, stream>>>(p);
-    else if (p.d_h == 64) rope_keys_kernel<3><<<grid, 256, 0, stream>>>(p);
-    else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    // a programmatic dependent of the stream's previous work: the launch
+    // overlaps that work's tail (the kernel waits for it before reading)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx > 0 ? gx : 1, gy > 0 ? gy : 1);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.d_h == 128) return cudaLaunchKernelEx(&cfg, rope_keys_kernel<4>, p);
+    if (p.d_h == 64) return cudaLaunchKernelEx(&cfg, rope_keys_kernel<3>, p);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace apex

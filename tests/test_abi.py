@@ -70,6 +70,27 @@ def test_fwd_rejects(lib, args, code):
     assert apex.apex_attn_fwd(*args, None) == code
 
 
+# empty and oversized problems: rejected on the host, nothing launched
+@pytest.mark.parametrize("args,code", [
+    ((FAKE, FAKE, FAKE, FAKE, 1, 4, 2, 0, 8, 64, 0, 0, 10000.0), 1),            # no query rows
+    ((FAKE, FAKE, FAKE, FAKE, 1, 4, 2, 0, 0, 64, 0, 0, 10000.0), 1),            # no keys
+    ((FAKE, FAKE, FAKE, FAKE, 1, 4, 2, 8, (1 << 24) + 1, 64, 0, 0, 10000.0), 2),  # beyond 2^24 keys
+    ((FAKE, FAKE, FAKE, FAKE, 0, 0, 0, 8, 8, 64, 0, 0, 10000.0), 1),            # no heads
+])
+def test_fwd_rejects_empty_and_oversized(lib, args, code):
+    assert apex.apex_attn_fwd(*args, None) == code
+
+
+def test_decode_rejects_empty_and_oversized(lib):
+    # no keys; beyond 2^24 keys
+    assert apex.apex_attn_decode(FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 0, 64, 0, 0, 10000.0, FAKE, 1 << 30, None) == 1
+    big = (1 << 24) + 1
+    assert apex.apex_attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 8, 2, big, 64, 0, big - 1, 10000.0, FAKE, 1 << 30,
+                                 None) == 2
+    assert apex.apex_attn_decode_workspace_bytes(1, 8, 2, big, 64) == 0
+    assert apex.fwd_workspace_bytes(1, 8, 2, 8, big, 128) == 0
+
+
 @pytest.mark.parametrize("args,code", [
     ((0, FAKE, FAKE, FAKE, 2, 8, 2, 64, 64, 0, 63, 10000.0, FAKE, 1 << 30), 1),
     ((FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 64, 64, 0, 64, 10000.0, FAKE, 1 << 30), 1),   # q_pos >= S_k

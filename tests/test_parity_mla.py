@@ -87,15 +87,33 @@ def test_mla_rope_part_zero_matches_oracle():
     _close(out, oracle.mla_attn(q, k, v, D_R, window=77), "mla content only")
 
 
-@pytest.mark.parametrize("rows", [[0, 1, 127, 128, 2047, 4095, 6000, 8191]])
-def test_mla_full_workload_sampled_rows(rows):
+def _item_rows(w, n_rand=48):
+    """One seeded row in each of the four M tiles of every work item of the
+    CTA-pair prefill (an item is 4 * 128 / G consecutive query rows of one
+    (batch, KV head) unit), plus the first and last 64 rows and random rows."""
+    P = 128 // w.G
+    rng = np.random.default_rng(20_000 + w.seed)
+    S = w.S_q
+    rows = set(range(64)) | set(range(S - 64, S)) | set(int(x) for x in rng.integers(0, S, n_rand))
+    for r0 in range(0, S, 4 * P):
+        for T in range(4):
+            lo = r0 + T * P
+            if lo < S:
+                rows.add(int(rng.integers(lo, min(lo + P, S))))
+    return sorted(rows)
+
+
+def test_mla_full_workload_every_item():
     """The global-layer MLA workload at full size, in the bench's launch
-    configuration, checked on sampled query rows of every head."""
+    configuration, checked on every head of a row set that touches every work
+    item and both tiles of each CTA of the pair kernel."""
     dev = _dev()
     w = inputs.WORKLOADS["mla"]
     q, k, v = inputs.workload_inputs(w)
     out = apex.mla_fwd(q.to(dev), k.to(dev), v.to(dev), w.d_r, window=w.window)
     torch.cuda.synchronize()
+    rows = _item_rows(w)
+    assert len(rows) >= w.S_q // (128 // w.G)
     got = out[:, :, rows].cpu()
     ref = oracle.mla_attn(q, k, v, w.d_r, window=w.window, rows=rows)
     _close(got, ref, "mla full")

@@ -68,19 +68,18 @@ MLA_PREFILL = [c for c in _prefill_cases(24, 20261204) if c[5] == 128][:10]
 MLA_DECODE = [c for c in _decode_cases(24, 20261205) if c[4] == 128][:10]
 
 
-@pytest.fixture(params=["pair", "single"])
-def kernel(request, monkeypatch):
+# every case through the single-CTA kernel, and the d_h = 128 ones (the rows the
+# CTA-pair kernel serves) through the pair kernel as well
+PREFILL_RUNS = [("single", c) for c in PREFILL] + [("pair", c) for c in PREFILL if c[5] == 128]
+
+
+@pytest.mark.parametrize("kernel,case", PREFILL_RUNS,
+                         ids=lambda x: x if isinstance(x, str) else "B%d_Hq%d_Hkv%d_Sq%d_Sk%d_d%d_p%d_W%d_P%d_y%g" % x)
+def test_prefill_fuzz(kernel, case, monkeypatch):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    monkeypatch.setenv("APEX_ATTN_PREFILL", request.param)
-    return request.param
-
-
-@pytest.mark.parametrize("case", PREFILL, ids=lambda c: "B%d_Hq%d_Hkv%d_Sq%d_Sk%d_d%d_p%d_W%d_P%d_y%g" % c)
-def test_prefill_fuzz(kernel, case):
+    monkeypatch.setenv("APEX_ATTN_PREFILL", kernel)
     B, H_q, H_kv, S_q, S_k, d, q_pos0, window, prefix, yarn = case
-    if kernel == "pair" and d != 128:
-        pytest.skip("the pair kernel serves d_h = 128")
     dev = torch.device("cuda:0")
     q, k, v = inputs.make_qkv(B, H_q, H_kv, S_q, S_k, d, 5000 + S_q + 7 * S_k)
     out = apex.fwd(q.to(dev), k.to(dev), v.to(dev), window=window, q_pos0=q_pos0, prefix_len=prefix,

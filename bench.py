@@ -30,7 +30,9 @@ Reported (one JSON line on rank 0):
            long: B1 H_q32 H_kv8 S65536 W4096; mla: the wide shape with 64-entry
            decoupled RoPE), each timed on its own after the step (same K and
            warm-up, CUDA events around every call) with its ms per call,
-           TFLOP/s and fraction of the measured bf16 peak.
+           TFLOP/s and fraction of the measured bf16 peak; all three rotate
+           their keys (for mla: the rope parts) once before the prefill kernel,
+           as the gqa call does, and the time covers both kernels.
 
 With --impl reference the oracle itself is the timed arm (host cores, bounded
 sample per step); it prints the same keys with "impl": "reference".
@@ -344,14 +346,13 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     feat = FEATURES[args.feature]
-    if (wp.d_r or wd.d_r) and feat.get("keys_prerotated"):
-        raise SystemExit("--feature prerotated rotates whole key rows; not defined for the decoupled-RoPE workload")
     if feat.get("keys_prerotated"):
-        # the caches hold RoPE(k_j, j): rotate the keys once, outside the timing
+        # the caches hold RoPE(k_j, j) (decoupled RoPE: the rope part rotated):
+        # rotate the keys once, outside the timing
         if do_pre:
-            pk = apex.rope_keys(pk)
+            pk = apex.mla_rope_keys(pk, wp.d_r) if wp.d_r else apex.rope_keys(pk)
         if do_dec:
-            dk = apex.rope_keys(dk)
+            dk = apex.mla_rope_keys(dk, wd.d_r) if wd.d_r else apex.rope_keys(dk)
         torch.cuda.synchronize()
 
     def prefill():
@@ -610,12 +611,14 @@ def prefill_call(apex, w, q, k, v, out, feat):
 def prefill_kernel_name(w, feat=None):
     """The prefill kernel a call runs, and whether the keys are rotated once by
     rope_keys_kernel before it (the call's time covers both)."""
-    if w.d_r:
-        return "prefill_pair_kernel", False
     import transformer_attention_rope_gb300 as apex
+    opts = {k: v for k, v in (feat or {}).items()}
+    if w.d_r:
+        prerot = apex.mla_fwd_workspace_bytes(w.B, w.H_q, w.H_kv, w.S_q, w.S_k, w.d_h, w.d_r, window=w.window,
+                                              q_pos0=w.q_pos0, rope_base=w.rope_base, **opts) > 0
+        return "prefill_pair_kernel", prerot
     name = ("prefill_kernel" if (w.d_h != 128 or os.environ.get("APEX_ATTN_PREFILL") == "single")
             else "prefill_pair_kernel")
-    opts = {k: v for k, v in (feat or {}).items()}
     prerot = apex.fwd_workspace_bytes(w.B, w.H_q, w.H_kv, w.S_q, w.S_k, w.d_h, window=w.window, q_pos0=w.q_pos0,
                                       rope_base=w.rope_base, **opts) > 0
     return name, prerot

@@ -180,6 +180,33 @@ apex_status apex_attn_mla_fwd(const void *q, const void *k, const void *v, void 
                               const apex_attn_options *opt, apex_stream_t stream);
 
 /*
+ * Bytes of caller-provided device workspace apex_attn_mla_fwd_ws will use for
+ * this call (same arguments): one copy of the key rows with the rope part
+ * rotated, B * H_kv * S_k * (d_h + d_r) bf16 values, when the library's cost
+ * model rotates the keys before the prefill; 0 when it would not, when
+ * opt->keys_prerotated is set, and when the arguments are invalid or
+ * unsupported.  Host-only, no CUDA call.
+ */
+size_t apex_attn_mla_fwd_workspace_bytes(int B, int H_q, int H_kv, int S_q, int S_k, int d_h, int d_r,
+                                         const apex_attn_options *opt);
+
+/*
+ * Decoupled-RoPE prefill with a workspace: the same result as apex_attn_mla_fwd
+ * (up to the order of fp32 sums), with the rope part of every key row rotated
+ * once into the workspace beforehand (as apex_attn_mla_rope_keys computes it;
+ * the content part copied) when the cost model says that is faster than
+ * rotating it in every work item that visits the key tile.  workspace and
+ * workspace_bytes as for apex_attn_fwd_ws, sized by
+ * apex_attn_mla_fwd_workspace_bytes(...); NULL makes this apex_attn_mla_fwd.
+ * Errors as for apex_attn_mla_fwd, plus APEX_ERR_INVALID_ARG for a smaller or
+ * misaligned workspace (before any launch).
+ */
+apex_status apex_attn_mla_fwd_ws(const void *q, const void *k, const void *v, void *out,
+                                 int B, int H_q, int H_kv, int S_q, int S_k, int d_h, int d_r,
+                                 const apex_attn_options *opt, void *workspace, size_t workspace_bytes,
+                                 apex_stream_t stream);
+
+/*
  * Decode with options: as apex_attn_decode, with window, q_pos and rope_base
  * taken from *opt.  With a prefix and q_pos < P the query sees keys [0, P).
  * The workspace size is apex_attn_decode_workspace_bytes(...) as for
@@ -233,6 +260,22 @@ apex_status apex_attn_mla_decode(const void *q, const void *k_cache, const void 
 apex_status apex_attn_rope_keys(const void *k_in, void *k_out, int n_heads, int n_pos, int d_h, int pos0,
                                 long long in_head_stride, long long out_head_stride,
                                 const apex_attn_options *opt, apex_stream_t stream);
+
+/*
+ * The same for decoupled-RoPE key rows [content (d_h) | rope part (d_r)]
+ * (Part 2 §9.3): for each head h and s < n_pos the row at
+ * k_in[h * in_head_stride + s * (d_h + d_r)] goes to k_out with its content
+ * part copied and its rope part rotated as a d_r-dimensional RoPE vector at
+ * position pos0 + s (pairs numbered from the rope part's start,
+ * theta_i = b^(-2i/d_r), the options' YaRN rule) -- the keys
+ * apex_attn_mla_fwd / apex_attn_mla_decode take with opt->keys_prerotated.
+ * Strides in elements (at least n_pos * (d_h + d_r), multiples of 8), overlap
+ * rules as for apex_attn_rope_keys.  Supported: d_h = 128, d_r = 64 (else
+ * APEX_ERR_UNSUPPORTED); d_r must be even and > 0 (else APEX_ERR_INVALID_ARG).
+ */
+apex_status apex_attn_mla_rope_keys(const void *k_in, void *k_out, int n_heads, int n_pos, int d_h, int d_r,
+                                    int pos0, long long in_head_stride, long long out_head_stride,
+                                    const apex_attn_options *opt, apex_stream_t stream);
 
 /*
  * Bytes of caller-provided device workspace apex_attn_decode needs for these

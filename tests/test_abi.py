@@ -187,6 +187,54 @@ def test_mla_fwd_rejects(lib, shape, code):
     assert apex.apex_attn_mla_fwd(0, FAKE, FAKE, FAKE, *shape, _opt(), None) == 1
 
 
+# decoupled-RoPE prefill with a workspace: (B, H_q, H_kv, S_q, S_k, d_h, d_r), options, workspace, bytes, status
+MLA_KEYS = 8 * 8192 * 192 * 2  # one bf16 copy of the key rows of B1 H_kv8 S8192 [128 | 64]
+
+
+@pytest.mark.parametrize("shape,opt,ws,nbytes,code", [
+    ((1, 4, 2, 8, 8, 128, 64), None, FAKE, 1 << 20, 1),                 # no options
+    ((1, 128, 8, 8192, 8192, 128, 64), {}, FAKE + 8, MLA_KEYS, 1),      # misaligned workspace
+    ((1, 128, 8, 8192, 8192, 128, 64), {}, FAKE, MLA_KEYS - 16, 1),     # one row short of the keys
+    ((1, 4, 2, 8, 8, 128, 63), {}, FAKE, 1 << 20, 1),                   # odd rope part
+    ((1, 4, 2, 8, 8, 64, 64), {}, FAKE, 1 << 20, 2),                    # only d_h = 128 with d_r = 64
+    ((1, 4, 2, 9, 8, 128, 64), {}, FAKE, 1 << 20, 1),                   # S_q > S_k
+])
+def test_mla_fwd_ws_rejects(lib, shape, opt, ws, nbytes, code):
+    o = None if opt is None else _opt(**opt)
+    assert apex.apex_attn_mla_fwd_ws(FAKE, FAKE, FAKE, FAKE, *shape, o, ws, nbytes, None) == code
+
+
+def test_mla_fwd_workspace_bytes(lib):
+    # one bf16 copy of the key rows where the pass pays (wide head groups, long windows) ...
+    assert apex.mla_fwd_workspace_bytes(1, 128, 8, 8192, 8192, 128, 64) == MLA_KEYS
+    assert apex.mla_fwd_workspace_bytes(1, 32, 8, 65536, 65536, 128, 64, window=4096) == 8 * 65536 * 192 * 2
+    # ... none where each key tile is visited a few times only (the rope part is a
+    # third of the row, so the in-kernel rotation costs less than for plain rows),
+    # for pre-rotated keys, and for bad or unsupported sizes
+    assert apex.mla_fwd_workspace_bytes(4, 32, 8, 4096, 4096, 128, 64, window=1024) == 0
+    assert apex.mla_fwd_workspace_bytes(1, 4, 2, 256, 256, 128, 64) == 0
+    assert apex.mla_fwd_workspace_bytes(1, 128, 8, 8192, 8192, 128, 64, keys_prerotated=True) == 0
+    assert apex.mla_fwd_workspace_bytes(1, 128, 8, 8192, 8192, 64, 64) == 0
+    assert apex.mla_fwd_workspace_bytes(1, 128, 8, 8192, 8192, 128, 0) == 0
+    assert apex.mla_fwd_workspace_bytes(1, 128, 8, 8192, 8000, 128, 64) == 0   # S_q > S_k
+    assert apex.apex_attn_mla_fwd_workspace_bytes(1, 128, 8, 8192, 8192, 128, 64, None) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    ((FAKE, FAKE, 2, 8, 128, 0, 0, 1536, 1536), 1),        # no rope part
+    ((FAKE, FAKE, 2, 8, 128, 63, 0, 1528, 1528), 1),       # odd rope part
+    ((FAKE, FAKE, 2, 8, 64, 64, 0, 1024, 1024), 2),        # only d_h = 128 with d_r = 64
+    ((FAKE, FAKE, 2, 8, 128, 32, 0, 1280, 1280), 2),
+    ((FAKE, FAKE, 0, 8, 128, 64, 0, 1536, 1536), 1),       # no heads
+    ((FAKE, FAKE, 2, 8, 128, 64, -1, 1536, 1536), 1),      # negative first position
+    ((FAKE, FAKE, 2, 8, 128, 64, 0, 1024, 1536), 1),       # input heads overlap (stride < 8 rows)
+    ((FAKE + 8, FAKE, 2, 8, 128, 64, 0, 1536, 1536), 1),   # misaligned input
+])
+def test_mla_rope_keys_rejects(lib, args, code):
+    assert apex.apex_attn_mla_rope_keys(*args, _opt(), None) == code
+    assert apex.apex_attn_mla_rope_keys(FAKE, FAKE, 2, 8, 128, 64, 0, 1536, 1536, None, None) == 1
+
+
 # decodes with options: (B, H_q, H_kv, S_k, d_h), options, workspace bytes, expected status
 @pytest.mark.parametrize("shape,opt,ws,code", [
     ((2, 8, 2, 64, 64), None, 1 << 30, 1),

@@ -118,3 +118,30 @@ def test_prefill_with_key_pass_writes_only_its_output_and_workspace(monkeypatch,
     apex.fwd(q, k, v, window=window, out=out, workspace=ws.view(torch.uint8))
     assert _guards_intact(obuf) and _guards_intact(wbuf)
     assert torch.isfinite(out.float()).all()
+
+
+def test_mla_prefill_with_key_pass_writes_only_its_output_and_workspace():
+    """The same for the decoupled-RoPE prefill: the pass over [content | rope part]
+    key rows writes only inside the workspace, the prefill only inside its output."""
+    dev = _dev()
+    B, H_q, H_kv, S, d, d_r = 1, 32, 2, 6000, 128, 64
+    nbytes = apex.mla_fwd_workspace_bytes(B, H_q, H_kv, S, S, d, d_r)
+    assert nbytes == B * H_kv * S * (d + d_r) * 2
+    q, k, v = [t.to(dev) for t in inputs.make_qkv(B, H_q, H_kv, S, S, d, 3300 + S, d_r=d_r)]
+    obuf, out = _guarded((B, H_q, S, d), dev)
+    wbuf, ws = _guarded((nbytes // 2,), dev)
+    apex.mla_fwd(q, k, v, d_r, out=out, workspace=ws.view(torch.uint8))
+    assert _guards_intact(obuf) and _guards_intact(wbuf)
+    assert torch.isfinite(out.float()).all()
+    assert apex.apex_attn_device_status() == 0
+
+
+def test_mla_rope_keys_writes_only_its_rows():
+    """apex_attn_mla_rope_keys appending rows into a cache writes only those rows."""
+    dev = _dev()
+    H, n, d = 3, 200, 192
+    src = inputs.normal_bf16((H, n, d), 3301, 1).to(dev)
+    obuf, out = _guarded((H, n, d), dev)
+    apex.mla_rope_keys(src.view(1, H, n, d), 64, pos0=500, out=out.view(1, H, n, d))
+    assert _guards_intact(obuf)
+    assert torch.isfinite(out.float()).all()

@@ -9,10 +9,11 @@ Raw C-ABI names (pointers and sizes):
     apex_attn_fwd, apex_attn_decode, apex_attn_decode_noalloc, apex_attn_decode_workspace_bytes,
     apex_attn_rope_reserve, apex_attn_device_status, apex_attn_status_string,
     apex_attn_fwd_ex, apex_attn_fwd_ws, apex_attn_fwd_workspace_bytes, apex_attn_decode_ex, apex_attn_rope_keys,
-    apex_attn_mla_fwd, apex_attn_mla_decode (with an Options struct)
+    apex_attn_mla_fwd, apex_attn_mla_fwd_ws, apex_attn_mla_fwd_workspace_bytes, apex_attn_mla_decode,
+    apex_attn_mla_rope_keys (with an Options struct)
 Tensor conveniences (torch, bf16, contiguous, on the current CUDA device):
     fwd(q, k, v, ...), decode(q, k_cache, v_cache, q_pos, ...), rope_keys(k, ...), mla_fwd(q, k, v, d_r, ...),
-    mla_decode(q, k_cache, v_cache, q_pos, d_r, ...)
+    mla_decode(q, k_cache, v_cache, q_pos, d_r, ...), mla_rope_keys(k, d_r, ...)
 """
 from __future__ import annotations
 
@@ -25,9 +26,10 @@ __all__ = [
     "apex_attn_decode_workspace_bytes", "apex_attn_rope_reserve", "apex_attn_device_status",
     "apex_attn_status_string", "apex_attn_fwd_ex", "apex_attn_fwd_ws", "apex_attn_fwd_workspace_bytes",
     "apex_attn_decode_ex", "apex_attn_rope_keys", "fwd_workspace_bytes",
-    "apex_attn_mla_fwd", "apex_attn_mla_decode", "apex_attn_selftest_wait_timeout", "Options", "fwd", "decode",
-    "decode_workspace_bytes",
-    "rope_keys", "mla_fwd", "mla_decode",
+    "apex_attn_mla_fwd", "apex_attn_mla_fwd_ws", "apex_attn_mla_fwd_workspace_bytes", "apex_attn_mla_decode",
+    "apex_attn_mla_rope_keys", "apex_attn_selftest_wait_timeout", "Options", "fwd", "decode",
+    "decode_workspace_bytes", "mla_fwd_workspace_bytes",
+    "rope_keys", "mla_fwd", "mla_decode", "mla_rope_keys",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -83,12 +85,18 @@ def load_library():
             lib.apex_attn_fwd_workspace_bytes.restype = sz
             lib.apex_attn_mla_fwd.argtypes = [vp, vp, vp, vp] + [i32] * 7 + [op, vp]
             lib.apex_attn_mla_fwd.restype = i32
+            lib.apex_attn_mla_fwd_ws.argtypes = [vp, vp, vp, vp] + [i32] * 7 + [op, vp, sz, vp]
+            lib.apex_attn_mla_fwd_ws.restype = i32
+            lib.apex_attn_mla_fwd_workspace_bytes.argtypes = [i32] * 7 + [op]
+            lib.apex_attn_mla_fwd_workspace_bytes.restype = sz
             lib.apex_attn_mla_decode.argtypes = [vp, vp, vp, vp] + [i32] * 6 + [op, vp, sz, vp]
             lib.apex_attn_mla_decode.restype = i32
             lib.apex_attn_decode_ex.argtypes = [vp, vp, vp, vp] + [i32] * 5 + [op, vp, sz, vp]
             lib.apex_attn_decode_ex.restype = i32
             lib.apex_attn_rope_keys.argtypes = [vp, vp] + [i32] * 4 + [ctypes.c_longlong] * 2 + [op, vp]
             lib.apex_attn_rope_keys.restype = i32
+            lib.apex_attn_mla_rope_keys.argtypes = [vp, vp] + [i32] * 5 + [ctypes.c_longlong] * 2 + [op, vp]
+            lib.apex_attn_mla_rope_keys.restype = i32
             lib.apex_attn_decode_workspace_bytes.argtypes = [i32] * 5
             lib.apex_attn_decode_workspace_bytes.restype = sz
             lib.apex_attn_rope_reserve.argtypes = [i32, i32, f32]
@@ -142,6 +150,18 @@ def apex_attn_mla_fwd(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, d_r, opt, strea
                                             ctypes.byref(opt) if opt is not None else None, stream)
 
 
+def apex_attn_mla_fwd_ws(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, d_r, opt, workspace, workspace_bytes,
+                         stream) -> int:
+    return load_library().apex_attn_mla_fwd_ws(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, d_r,
+                                               ctypes.byref(opt) if opt is not None else None, workspace,
+                                               workspace_bytes, stream)
+
+
+def apex_attn_mla_fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h, d_r, opt) -> int:
+    return load_library().apex_attn_mla_fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h, d_r,
+                                                            ctypes.byref(opt) if opt is not None else None)
+
+
 def apex_attn_mla_decode(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, d_r, opt, workspace,
                          workspace_bytes, stream) -> int:
     return load_library().apex_attn_mla_decode(q, k_cache, v_cache, out, B, H_q, H_kv, S_k, d_h, d_r,
@@ -161,6 +181,13 @@ def apex_attn_rope_keys(k_in, k_out, n_heads, n_pos, d_h, pos0, in_head_stride, 
     return load_library().apex_attn_rope_keys(k_in, k_out, n_heads, n_pos, d_h, pos0, in_head_stride,
                                               out_head_stride, ctypes.byref(opt) if opt is not None else None,
                                               stream)
+
+
+def apex_attn_mla_rope_keys(k_in, k_out, n_heads, n_pos, d_h, d_r, pos0, in_head_stride, out_head_stride, opt,
+                            stream) -> int:
+    return load_library().apex_attn_mla_rope_keys(k_in, k_out, n_heads, n_pos, d_h, d_r, pos0, in_head_stride,
+                                                  out_head_stride, ctypes.byref(opt) if opt is not None else None,
+                                                  stream)
 
 
 def apex_attn_decode_workspace_bytes(B, H_q, H_kv, S_k, d_h) -> int:
@@ -257,11 +284,25 @@ def fwd(q, k, v, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.0
     return out
 
 
+def mla_fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h, d_r, *, window: int = 0, q_pos0: int = 0,
+                            rope_base: float = 10000.0, yarn_scale: float = 1.0, yarn_beta_fast: float = 32.0,
+                            yarn_beta_slow: float = 1.0, prefix_len: int = 0, keys_prerotated: bool = False) -> int:
+    """Workspace bytes a decoupled-RoPE prefill with these arguments uses (0: none; see
+    apex_attn_mla_fwd_workspace_bytes)."""
+    opt = _options(window, q_pos0, rope_base, yarn_scale, yarn_beta_fast, yarn_beta_slow, prefix_len,
+                   keys_prerotated)
+    return int(apex_attn_mla_fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h, int(d_r), opt))
+
+
 def mla_fwd(q, k, v, d_r: int, *, window: int = 0, q_pos0: int = 0, rope_base: float = 10000.0, out=None,
             stream=None, yarn_scale: float = 1.0, yarn_beta_fast: float = 32.0, yarn_beta_slow: float = 1.0,
-            prefix_len: int = 0, keys_prerotated: bool = False):
+            prefix_len: int = 0, keys_prerotated: bool = False, workspace=None):
     """Decoupled-RoPE prefill. q [B,H_q,S_q,d_h+d_r], k [B,H_kv,S_k,d_h+d_r], v [B,H_kv,S_k,d_h]
-    (bf16, CUDA; rows [content | rope part]) -> out [B,H_q,S_q,d_h]."""
+    (bf16, CUDA; rows [content | rope part]) -> out [B,H_q,S_q,d_h].
+
+    workspace: None -- a buffer from torch's allocator when the library would rotate
+    the keys' rope parts once before the prefill (mla_fwd_workspace_bytes > 0); a
+    uint8 CUDA tensor -- that buffer; False -- no workspace (apex_attn_mla_fwd)."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check(t, n, 4)
@@ -274,10 +315,21 @@ def mla_fwd(q, k, v, d_r: int, *, window: int = 0, q_pos0: int = 0, rope_base: f
     _check(out, "out", 4)
     opt = _options(window, q_pos0, rope_base, yarn_scale, yarn_beta_fast, yarn_beta_slow, prefix_len,
                    keys_prerotated)
-    st = apex_attn_mla_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H_q, H_kv, S_q, S_k,
-                           d_h, int(d_r), opt, _stream_handle(stream))
+    if workspace is None:
+        need = int(apex_attn_mla_fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h, int(d_r), opt))
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is not None and workspace is not False:
+        st = apex_attn_mla_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H_q, H_kv, S_q,
+                                  S_k, d_h, int(d_r), opt, workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        name = "apex_attn_mla_fwd_ws"
+    else:
+        st = apex_attn_mla_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H_q, H_kv, S_q, S_k,
+                               d_h, int(d_r), opt, _stream_handle(stream))
+        name = "apex_attn_mla_fwd"
     if st != APEX_OK:
-        raise ApexError(st, "apex_attn_mla_fwd")
+        raise ApexError(st, name)
     return out
 
 
@@ -364,4 +416,24 @@ def rope_keys(k, *, pos0: int = 0, out=None, rope_base: float = 10000.0, yarn_sc
                              _stream_handle(stream))
     if st != APEX_OK:
         raise ApexError(st, "apex_attn_rope_keys")
+    return out
+
+
+def mla_rope_keys(k, d_r: int, *, pos0: int = 0, out=None, rope_base: float = 10000.0, yarn_scale: float = 1.0,
+                  yarn_beta_fast: float = 32.0, yarn_beta_slow: float = 1.0, stream=None):
+    """Decoupled-RoPE key rows k [B,H,S,d_h+d_r] (bf16, CUDA; [content | rope part]) with the
+    rope part rotated to positions pos0 + s and the content part copied (pre-rotated cache)."""
+    import torch
+    _check(k, "k", 4)
+    B, H, S, d = k.shape
+    if out is None:
+        out = torch.empty_like(k)
+    _check(out, "out", 4)
+    if out.shape != k.shape:
+        raise ValueError("out must have the shape of k")
+    opt = _options(0, 0, rope_base, yarn_scale, yarn_beta_fast, yarn_beta_slow)
+    st = apex_attn_mla_rope_keys(k.data_ptr(), out.data_ptr(), B * H, S, d - int(d_r), int(d_r), int(pos0), S * d,
+                                 S * d, opt, _stream_handle(stream))
+    if st != APEX_OK:
+        raise ApexError(st, "apex_attn_mla_rope_keys")
     return out

@@ -280,16 +280,26 @@ int max_stages_for(int S_k) { return (S_k + kDecodeKeysPerStage - 1) / kDecodeKe
 // by every item whose key range covers it, so it is rotated that many times
 // (about 9 on B4 H_q32 S4096 W1024, 33 on S65536 W4096, 130 on a G = 16
 // causal S8192).  Rotating the keys once into a workspace costs a read and a
-// write of K.  Measured on GB300: about 1.7 ns of kernel time per (item, key
-// tile) visit, against 10 ns per 128-key tile for the pass and about 1 us for
-// its launch (the prefill, a programmatic dependent, sets up during the pass);
-// the pass is used when it costs less than the visits it saves.
+// write of K.  Measured on GB300, plain 128-wide rows: about 1.7 ns of kernel
+// time per (item, key tile) visit, against 10 ns per 128-key tile for the pass
+// and about 1 us for its launch (the prefill, a programmatic dependent, sets up
+// during the pass); decoupled-RoPE rows (128 + 64, only the 64-entry rope part
+// turned): about 1.1 ns per visit against 15 ns per tile (1.5 times the bytes).
+// The pass is used when it costs less than the visits it saves.
 struct PrerotatePlan {
     bool use;
     int n_pos;  // keys rotated (whole 128-key tiles up to the last one any item reads)
 };
 
-PrerotatePlan plan_prerotate(int units, int S_q, int S_k, int q_pos0, int window, int P, int block_rows)
+// costs in units of 0.1 ns
+struct PrerotateCost {
+    int per_visit, per_tile;
+};
+constexpr PrerotateCost kCostPlain{17, 100};
+constexpr PrerotateCost kCostDecoupled{11, 150};
+
+PrerotatePlan plan_prerotate(int units, int S_q, int S_k, int q_pos0, int window, int P, int block_rows,
+                             PrerotateCost cost)
 {
     long long visits = 0;
     int kmax = 0;
@@ -304,7 +314,7 @@ PrerotatePlan plan_prerotate(int units, int S_q, int S_k, int q_pos0, int window
     const int n_pos = std::min(S_k, (kmax / 128 + 1) * 128);
     const long long tiles = (long long)units * ((n_pos + 127) / 128);
     visits *= units;
-    return PrerotatePlan{visits * 17 >= tiles * 100 + 10000, n_pos};
+    return PrerotatePlan{visits * cost.per_visit >= tiles * cost.per_tile + 10000, n_pos};
 }
 
 }  // namespace
@@ -528,11 +538,12 @@ apex_status prefill_launch(const void *q, const void *k, const void *v, void *ou
     const int G = H_q / H_kv;
     const int rows_per_head = 128 / G;
     const bool pair = mla || use_pair_prefill(d_qk, st->sm_count);
-    // keys rotated once into the workspace (plain block on CTA pairs) when that
-    // costs less than rotating them in every work item that visits them
+    // keys rotated once into the workspace when that costs less than rotating
+    // them in every work item that visits them
     PrerotatePlan pre{false, 0};
-    if (workspace && !mla && !opt->keys_prerotated)
-        pre = plan_prerotate(B * H_kv, S_q, S_k, q_pos0, window > 0 ? window : 0, P, (pair ? 4 : 2) * rows_per_head);
+    if (workspace && !opt->keys_prerotated)
+        pre = plan_prerotate(B * H_kv, S_q, S_k, q_pos0, window > 0 ? window : 0, P, (pair ? 4 : 2) * rows_per_head,
+                             mla ? kCostDecoupled : kCostPlain);
     PrefillLaunch L;
     memset(&L, 0, sizeof L);
     if (!make_map(&L.tm_q, q, d_qk, S_q, B * H_q, rows_per_head, G) ||
@@ -547,7 +558,8 @@ apex_status prefill_launch(const void *q, const void *k, const void *v, void *ou
         rp.in_stride = rp.out_stride = (long long)S_k * d_qk;
         rp.n_heads = B * H_kv;
         rp.n_pos = pre.n_pos;
-        rp.d_h = d_qk;
+        rp.d_row = d_qk;
+        rp.d_rot = d_rope;
         rp.pos0 = 0;
         rp.rope = tv;
         if (launch_rope_keys(rp, st->sm_count, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -596,19 +608,36 @@ apex_status apex_attn_fwd_ex(const void *q, const void *k, const void *v, void *
     return prefill_launch(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, d_h, d_h, opt, f, stream);
 }
 
-size_t apex_attn_fwd_workspace_bytes(int B, int H_q, int H_kv, int S_q, int S_k, int d_h,
-                                     const apex_attn_options *opt)
+// Workspace of the key-rotation pass (0: the pass would not run); d_r = 0 for
+// the plain block, else the rope part of decoupled-RoPE rows [d_h | d_r].
+static size_t prefill_workspace_bytes(int B, int H_q, int H_kv, int S_q, int S_k, int d_h, int d_r,
+                               const apex_attn_options *opt)
 {
     if (!opt || opt->keys_prerotated) return 0;
     RopeFreq f;
     if (!freq_of(*opt, &f) || check_common(B, H_q, H_kv, S_k, d_h, f.base) != APEX_OK) return 0;
+    if (d_r != 0 && (d_h != 128 || d_r != 64)) return 0;
     const int q_pos0 = opt->q_pos, P = opt->prefix_len;
     if (S_q <= 0 || q_pos0 < 0 || (long long)q_pos0 + S_q > (long long)S_k || P < 0 || P > S_k) return 0;
     // a work item covers 4 M tiles of 128 / G query rows on CTA pairs, 2 on one CTA
-    const int block_rows = (use_pair_prefill(d_h, 2) ? 4 : 2) * (128 / (H_q / H_kv));
+    const bool pair = d_r != 0 || use_pair_prefill(d_h, 2);
+    const int block_rows = (pair ? 4 : 2) * (128 / (H_q / H_kv));
     const PrerotatePlan pr = plan_prerotate(B * H_kv, S_q, S_k, q_pos0, opt->window > 0 ? opt->window : 0, P,
-                                            block_rows);
-    return pr.use ? (size_t)B * H_kv * (size_t)S_k * d_h * 2 : 0;
+                                            block_rows, d_r ? kCostDecoupled : kCostPlain);
+    return pr.use ? (size_t)B * H_kv * (size_t)S_k * (d_h + d_r) * 2 : 0;
+}
+
+size_t apex_attn_fwd_workspace_bytes(int B, int H_q, int H_kv, int S_q, int S_k, int d_h,
+                                     const apex_attn_options *opt)
+{
+    return prefill_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h, 0, opt);
+}
+
+size_t apex_attn_mla_fwd_workspace_bytes(int B, int H_q, int H_kv, int S_q, int S_k, int d_h, int d_r,
+                                         const apex_attn_options *opt)
+{
+    if (d_r <= 0) return 0;
+    return prefill_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h, d_r, opt);
 }
 
 apex_status apex_attn_fwd_ws(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
@@ -627,8 +656,9 @@ apex_status apex_attn_fwd_ws(const void *q, const void *k, const void *v, void *
     return prefill_launch(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, d_h, d_h, opt, f, stream, workspace);
 }
 
-apex_status apex_attn_mla_fwd(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
-                              int S_q, int S_k, int d_h, int d_r, const apex_attn_options *opt, apex_stream_t stream)
+apex_status apex_attn_mla_fwd_ws(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
+                                 int S_q, int S_k, int d_h, int d_r, const apex_attn_options *opt, void *workspace,
+                                 size_t workspace_bytes, apex_stream_t stream)
 {
     if (!q || !k || !v || !out || !opt) return APEX_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return APEX_ERR_INVALID_ARG;
@@ -638,7 +668,16 @@ apex_status apex_attn_mla_fwd(const void *q, const void *k, const void *v, void 
     apex_status s = check_common(B, H_q, H_kv, S_k, d_h, f.base);
     if (s != APEX_OK) return s;
     if (d_h != 128 || d_r != 64) return APEX_ERR_UNSUPPORTED;
-    return prefill_launch(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h + d_r, d_h, d_r, opt, f, stream);
+    if (workspace && (!aligned16(workspace) ||
+                      workspace_bytes < apex_attn_mla_fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, d_h, d_r, opt)))
+        return APEX_ERR_INVALID_ARG;
+    return prefill_launch(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h + d_r, d_h, d_r, opt, f, stream, workspace);
+}
+
+apex_status apex_attn_mla_fwd(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
+                              int S_q, int S_k, int d_h, int d_r, const apex_attn_options *opt, apex_stream_t stream)
+{
+    return apex_attn_mla_fwd_ws(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, d_r, opt, nullptr, 0, stream);
 }
 
 apex_status apex_attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H_q, int H_kv,
@@ -653,15 +692,16 @@ apex_status apex_attn_fwd(const void *q, const void *k, const void *v, void *out
     return apex_attn_fwd_ex(q, k, v, out, B, H_q, H_kv, S_q, S_k, d_h, &o, stream);
 }
 
-apex_status apex_attn_rope_keys(const void *k_in, void *k_out, int n_heads, int n_pos, int d_h, int pos0,
-                                long long in_head_stride, long long out_head_stride,
-                                const apex_attn_options *opt, apex_stream_t stream)
+// Rows of d_row entries whose trailing d_rot entries are rotated (d_rot = d_row:
+// the plain block; d_rot < d_row: the rope part of decoupled-RoPE rows).
+static apex_status rope_keys_launch(const void *k_in, void *k_out, int n_heads, int n_pos, int d_row, int d_rot, int pos0,
+                             long long in_head_stride, long long out_head_stride, const apex_attn_options *opt,
+                             apex_stream_t stream)
 {
     if (!k_in || !k_out || !opt) return APEX_ERR_INVALID_ARG;
     if (!aligned16(k_in) || !aligned16(k_out)) return APEX_ERR_INVALID_ARG;
     if (n_heads <= 0 || n_pos <= 0 || pos0 < 0) return APEX_ERR_INVALID_ARG;
-    if (d_h != 64 && d_h != 128) return APEX_ERR_UNSUPPORTED;
-    if (in_head_stride < (long long)n_pos * d_h || out_head_stride < (long long)n_pos * d_h ||
+    if (in_head_stride < (long long)n_pos * d_row || out_head_stride < (long long)n_pos * d_row ||
         (in_head_stride % 8) != 0 || (out_head_stride % 8) != 0)
         return APEX_ERR_INVALID_ARG;
     if ((long long)pos0 + n_pos > kMaxSeq) return APEX_ERR_UNSUPPORTED;
@@ -674,7 +714,7 @@ apex_status apex_attn_rope_keys(const void *k_in, void *k_out, int n_heads, int 
     apex_status s = init_device(*st, dev);
     if (s != APEX_OK) return s;
     RopeTableView tv;
-    s = get_table(*st, d_h, f, pos0 + n_pos, &tv);
+    s = get_table(*st, d_rot, f, pos0 + n_pos, &tv);
     if (s != APEX_OK) return s;
     RopeKeysParams p;
     p.in = static_cast<const uint16_t *>(k_in);
@@ -683,12 +723,32 @@ apex_status apex_attn_rope_keys(const void *k_in, void *k_out, int n_heads, int 
     p.out_stride = out_head_stride;
     p.n_heads = n_heads;
     p.n_pos = n_pos;
-    p.d_h = d_h;
+    p.d_row = d_row;
+    p.d_rot = d_rot;
     p.pos0 = pos0;
     p.rope = tv;
     if (launch_rope_keys(p, st->sm_count, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return APEX_ERR_CUDA;
     return APEX_OK;
+}
+
+apex_status apex_attn_rope_keys(const void *k_in, void *k_out, int n_heads, int n_pos, int d_h, int pos0,
+                                long long in_head_stride, long long out_head_stride,
+                                const apex_attn_options *opt, apex_stream_t stream)
+{
+    if (d_h != 64 && d_h != 128) return APEX_ERR_UNSUPPORTED;
+    return rope_keys_launch(k_in, k_out, n_heads, n_pos, d_h, d_h, pos0, in_head_stride, out_head_stride, opt,
+                            stream);
+}
+
+apex_status apex_attn_mla_rope_keys(const void *k_in, void *k_out, int n_heads, int n_pos, int d_h, int d_r,
+                                    int pos0, long long in_head_stride, long long out_head_stride,
+                                    const apex_attn_options *opt, apex_stream_t stream)
+{
+    if (d_r <= 0 || (d_r & 1)) return APEX_ERR_INVALID_ARG;
+    if (d_h != 128 || d_r != 64) return APEX_ERR_UNSUPPORTED;
+    return rope_keys_launch(k_in, k_out, n_heads, n_pos, d_h + d_r, d_r, pos0, in_head_stride, out_head_stride,
+                            opt, stream);
 }
 
 }  // extern "C"

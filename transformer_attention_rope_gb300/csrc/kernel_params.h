@@ -101,7 +101,9 @@ struct RopeKeysParams {
     const uint16_t *in;
     uint16_t *out;
     long long in_stride, out_stride;  // elements between heads
-    int n_heads, n_pos, d_h, pos0;
+    int n_heads, n_pos, pos0;
+    int d_row;  // entries per key row
+    int d_rot;  // trailing entries of a row that are rotated (the rest are copied)
     RopeTableView rope;
 };
 

@@ -153,3 +153,37 @@ def test_mla_prerotated_cache_prefill_and_decode():
     mx, mean = _errs(o1.cpu(), ref)
     assert mx <= MAX_ERR and mean <= MEAN_ERR, (mx, mean)
     assert apex.apex_attn_device_status() == 0
+
+
+def test_mla_pass_and_prefill_captured_in_a_graph():
+    """The decoupled-RoPE pass and the prefill launched as its programmatic
+    dependent, captured in one CUDA graph and replayed on new inputs copied into
+    the same buffers."""
+    dev = _dev()
+    B, H_q, H_kv, S = 1, 32, 2, 4096
+    assert apex.mla_fwd_workspace_bytes(B, H_q, H_kv, S, S, D_H, D_R) > 0
+    q, k, v = (t.to(dev) for t in inputs.make_qkv(B, H_q, H_kv, S, S, D_H, 9100, d_r=D_R))
+    out = torch.empty((B, H_q, S, D_H), dtype=torch.bfloat16, device=dev)
+    ws = _ws(B, H_kv, S, dev)
+    apex.mla_fwd(q, k, v, D_R, out=out, workspace=ws)  # table built, module loaded
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            apex.mla_fwd(q, k, v, D_R, out=out, workspace=ws, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    rows = _rows(S, 11)
+    for seed in (9101, 9102):
+        qh, kh, vh = inputs.make_qkv(B, H_q, H_kv, S, S, D_H, seed, d_r=D_R)
+        q.copy_(qh)
+        k.copy_(kh)
+        v.copy_(vh)
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.mla_attn(qh, kh, vh, D_R, rows=rows)
+        mx, mean = _errs(out[:, :, rows].cpu(), ref)
+        assert mx <= MAX_ERR and mean <= MEAN_ERR, (seed, mx, mean)
+    assert apex.apex_attn_device_status() == 0

@@ -187,3 +187,30 @@ def test_mla_pass_and_prefill_captured_in_a_graph():
         mx, mean = _errs(out[:, :, rows].cpu(), ref)
         assert mx <= MAX_ERR and mean <= MEAN_ERR, (seed, mx, mean)
     assert apex.apex_attn_device_status() == 0
+
+
+def test_mla_pass_on_a_chunk_of_a_longer_sequence():
+    """Rows at positions 3000..6999 against 9001 key rows (the last 2001 never
+    visible): the pass rotates the key rows up to the end of the last 128-key
+    tile any work item reads, leaves the rest of the workspace as it was, and
+    the output matches the oracle."""
+    dev = _dev()
+    B, H_q, H_kv, S_q, S_k, q_pos0 = 1, 32, 2, 4000, 9001, 3000
+    assert apex.mla_fwd_workspace_bytes(B, H_q, H_kv, S_q, S_k, D_H, D_R, q_pos0=q_pos0) > 0
+    q = inputs.normal_bf16((B, H_q, S_q, D_H + D_R), 9200, 0)
+    k = inputs.normal_bf16((B, H_kv, S_k, D_H + D_R), 9200, 1)
+    v = inputs.normal_bf16((B, H_kv, S_k, D_H), 9200, 2)
+    kd = k.to(dev)
+    ws = _ws(B, H_kv, S_k, dev)
+    out = apex.mla_fwd(q.to(dev), kd, v.to(dev), D_R, q_pos0=q_pos0, workspace=ws)
+    torch.cuda.synchronize()
+    n_pos = ((q_pos0 + S_q - 1) // 128 + 1) * 128  # 7040
+    held = ws.view(torch.int16).view(B, H_kv, S_k, D_H + D_R)
+    rot = apex.mla_rope_keys(kd, D_R).view(torch.int16)
+    assert torch.equal(held[:, :, :n_pos], rot[:, :, :n_pos])
+    assert bool((held[:, :, n_pos:] == NAN_BF16).all())
+    rows = _rows(S_q, 9)
+    ref = oracle.mla_attn(q, k, v, D_R, q_pos0=q_pos0, rows=rows)
+    mx, mean = _errs(out[:, :, rows].cpu(), ref)
+    assert mx <= MAX_ERR and mean <= MEAN_ERR, (mx, mean)
+    assert apex.apex_attn_device_status() == 0

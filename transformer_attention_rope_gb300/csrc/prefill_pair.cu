@@ -370,8 +370,9 @@ __device__ __forceinline__ int item_index(int k)
     return k * g + ((k & 1) ? (g - 1 - c) : c);
 }
 
-// KROT: the K tiles are rotated in shared memory (unless p.keys_prerotated);
-// false: the instance for keys the library rotated once beforehand.
+// KROT: the K tiles are rotated in shared memory; false: the instance for keys
+// rotated beforehand (by the library's key pass or by the caller), at both row
+// widths.
 template <int DQK, int DR, bool KROT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -806,7 +807,8 @@ cudaError_t launch_prefill_pair(const PrefillLaunch &L, cudaStream_t stream)
     if (L.grid & 1) return cudaErrorInvalidValue;
     if (L.p.d_h == 128 && L.p.d_rope == 128)
         return L.p.keys_prerotated ? launch_pair_t<128, 128, false>(L, stream) : launch_pair_t<128, 128, true>(L, stream);
-    if (L.p.d_h == 192 && L.p.d_rope == 64) return launch_pair_t<192, 64, true>(L, stream);
+    if (L.p.d_h == 192 && L.p.d_rope == 64)
+        return L.p.keys_prerotated ? launch_pair_t<192, 64, false>(L, stream) : launch_pair_t<192, 64, true>(L, stream);
     return cudaErrorInvalidValue;
 }
 
